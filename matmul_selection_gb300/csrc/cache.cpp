@@ -1,0 +1,197 @@
+// On-disk tuning table.
+//
+// Format follows TunableOp's result file (PyTorch TunableOp guide, section
+// 3.2): "Validator,<NAME>,<value>" rows, then one row per result with the
+// operator, its parameters, the solution name and the time.  Here:
+//   MatmulKey,<canonical key text>,<candidate name>,<median ms>,<ranking>
+// where <ranking> lists "name:median_ms" of every valid candidate, fastest
+// first, separated by ';' -- kept so an entry can be inspected after the fact
+// (burn "autotune" page, section "cache: in-memory table and default.db").
+// Validators (mismatch of any one rejects the WHOLE file, as TunableOp's
+// ValidateAll does): MM_VERSION, CANDIDATE_CHECKSUM, DEVICE, CUDA_VERSION.
+// A row naming an unknown candidate is skipped; "Default" names the default
+// (naive) kernel, as TunableOp's hand-edit rule allows.
+#include <algorithm>
+#include <cstdio>
+#include <fstream>
+#include <sstream>
+
+#include "common.h"
+
+#ifndef MM_BUILD_ID
+#define MM_BUILD_ID "dev"
+#endif
+
+namespace mm {
+
+namespace {
+
+std::vector<std::pair<std::string, std::string>> validators(const DeviceState &ds) {
+  char cks[32];
+  snprintf(cks, sizeof cks, "%016llx", (unsigned long long)registry_checksum());
+  int rt = 0;
+  cudaRuntimeGetVersion(&rt);
+  char dev[256];
+  snprintf(dev, sizeof dev, "%s|sm_%d%d|%s", ds.info.name.c_str(), ds.info.cc_major,
+           ds.info.cc_minor, ds.info.uuid.c_str());
+  return {{"MM_VERSION", std::string(kVersion) + "+" + MM_BUILD_ID},
+          {"CANDIDATE_CHECKSUM", cks},
+          {"DEVICE", dev},
+          {"CUDA_VERSION", std::to_string(rt)}};
+}
+
+// CSV fields: a field holding ',' or '"' is written in double quotes with
+// embedded quotes doubled (the key text contains commas).
+std::string csv_field(const std::string &f) {
+  if (f.find_first_of(",\"") == std::string::npos) return f;
+  std::string q = "\"";
+  for (char c : f) {
+    if (c == '"') q += '"';
+    q += c;
+  }
+  return q + "\"";
+}
+
+std::vector<std::string> csv_split(const std::string &s) {
+  std::vector<std::string> out;
+  std::string cur;
+  bool quoted = false;
+  for (size_t i = 0; i < s.size(); ++i) {
+    char c = s[i];
+    if (quoted) {
+      if (c == '"') {
+        if (i + 1 < s.size() && s[i + 1] == '"') {
+          cur += '"';
+          ++i;
+        } else {
+          quoted = false;
+        }
+      } else {
+        cur += c;
+      }
+    } else if (c == '"') {
+      quoted = true;
+    } else if (c == ',') {
+      out.push_back(cur);
+      cur.clear();
+    } else {
+      cur += c;
+    }
+  }
+  out.push_back(cur);
+  return out;
+}
+
+std::vector<std::string> split(const std::string &s, char d, size_t max_fields) {
+  std::vector<std::string> out;
+  size_t start = 0;
+  while (out.size() + 1 < max_fields) {
+    size_t c = s.find(d, start);
+    if (c == std::string::npos) break;
+    out.push_back(s.substr(start, c - start));
+    start = c + 1;
+  }
+  out.push_back(s.substr(start));
+  return out;
+}
+
+int candidate_index(const std::string &name) {
+  if (name == "Default") return 0;
+  const auto &reg = registry();
+  for (int i = 0; i < (int)reg.size(); ++i)
+    if (reg[i].name == name) return i;
+  return -1;
+}
+
+}  // namespace
+
+std::string device_file_name(const std::string &path, int ordinal) {
+  size_t slash = path.find_last_of('/');
+  size_t dot = path.find_last_of('.');
+  std::string ord = std::to_string(ordinal);
+  if (dot == std::string::npos || (slash != std::string::npos && dot < slash))
+    return path + ord;
+  return path.substr(0, dot) + ord + path.substr(dot);
+}
+
+mm_status cache_load(DeviceState &ds, const std::string &path) {
+  std::ifstream f(path);
+  if (!f) return set_error(MM_ERR_IO, "cannot open '%s'", path.c_str());
+  std::map<std::string, std::string> seen;
+  std::vector<std::vector<std::string>> rows;
+  std::string line;
+  while (std::getline(f, line)) {
+    if (!line.empty() && line.back() == '\r') line.pop_back();
+    if (line.empty()) continue;
+    if (line.rfind("Validator,", 0) == 0) {
+      auto v = split(line, ',', 3);
+      if (v.size() == 3) seen[v[1]] = v[2];
+      continue;
+    }
+    rows.push_back(csv_split(line));
+  }
+  for (const auto &kv : validators(ds)) {
+    auto it = seen.find(kv.first);
+    if (it == seen.end())
+      return set_error(MM_ERR_CACHE_VALIDATION, "'%s': validator %s missing", path.c_str(),
+                       kv.first.c_str());
+    if (it->second != kv.second)
+      return set_error(MM_ERR_CACHE_VALIDATION, "'%s': validator %s is '%s', expected '%s'",
+                       path.c_str(), kv.first.c_str(), it->second.c_str(), kv.second.c_str());
+  }
+  std::unique_lock<std::shared_mutex> lk(ds.table_mu);
+  for (const auto &r : rows) {
+    if (r.size() < 3 || r[0] != "MatmulKey") continue;
+    KeyPod k;
+    if (!parse_key_text(r[1], &k)) continue;
+    int w = candidate_index(r[2]);
+    if (w < 0) continue;  // unknown solution name: skip this row
+    if (ds.table.count(k)) continue;
+    TableEntry e;
+    e.winner = w;
+    e.ranking.push_back(w);
+    e.median_ms = r.size() > 3 ? atof(r[3].c_str()) : 0.0;
+    if (r.size() > 4) {
+      e.detail = r[4];
+      for (const auto &tok : split(r[4], ';', 1 << 20)) {
+        size_t c = tok.rfind(':');
+        int i = candidate_index(tok.substr(0, c));
+        if (i >= 0 && std::find(e.ranking.begin(), e.ranking.end(), i) == e.ranking.end())
+          e.ranking.push_back(i);
+      }
+    }
+    if (std::find(e.ranking.begin(), e.ranking.end(), 0) == e.ranking.end()) e.ranking.push_back(0);
+    e.from_file = true;
+    ds.table[k] = e;
+  }
+  return MM_OK;
+}
+
+mm_status cache_save(DeviceState &ds, const std::string &path) {
+  std::vector<std::string> lines;
+  {
+    std::shared_lock<std::shared_mutex> lk(ds.table_mu);
+    for (const auto &kv : ds.table) {
+      const TableEntry &e = kv.second;
+      char ms[64];
+      snprintf(ms, sizeof ms, "%.6g", e.median_ms);
+      lines.push_back("MatmulKey," + csv_field(key_text(kv.first)) + "," +
+                      csv_field(registry()[e.winner].name) + "," + ms + "," + csv_field(e.detail));
+    }
+  }
+  std::sort(lines.begin(), lines.end());
+  std::string tmp = path + ".tmp";
+  {
+    std::ofstream f(tmp, std::ios::trunc);
+    if (!f) return set_error(MM_ERR_IO, "cannot write '%s'", tmp.c_str());
+    for (const auto &kv : validators(ds)) f << "Validator," << kv.first << "," << kv.second << "\n";
+    for (const auto &l : lines) f << l << "\n";
+    if (!f) return set_error(MM_ERR_IO, "write to '%s' failed", tmp.c_str());
+  }
+  if (std::rename(tmp.c_str(), path.c_str()) != 0)
+    return set_error(MM_ERR_IO, "cannot rename '%s' to '%s'", tmp.c_str(), path.c_str());
+  ds.dirty = false;
+  return MM_OK;
+}
+
+}  // namespace mm

@@ -1,0 +1,270 @@
+// Internal declarations of the GB300 autotuned matmul library.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <condition_variable>
+#include <cstdint>
+#include <cstring>
+#include <map>
+#include <memory>
+#include <mutex>
+#include <shared_mutex>
+#include <string>
+#include <unordered_map>
+#include <unordered_set>
+#include <vector>
+
+#include "../../include/mm.h"
+
+namespace mm {
+
+constexpr const char *kVersion = "0.1.0";
+
+// ---------------------------------------------------------------- problem
+struct Problem {
+  const void *A;
+  const void *B;
+  void *C;
+  int64_t M, N, K;
+  int64_t lda, ldb, ldc;
+  int64_t batch;
+  int64_t sA, sB, sC;  // batch strides, elements
+  int ta, tb, tc;      // mm_dtype of A, B, C
+  bool at, bt;         // A / B stored transposed (layout letter T)
+};
+
+inline int dtype_bytes(int t) { return t == MM_F32 ? 4 : 2; }
+inline const char *dtype_name(int t) {
+  return t == MM_BF16 ? "bf16" : t == MM_F16 ? "f16" : t == MM_F32 ? "f32" : "?";
+}
+
+// Elements from the first to one past the last element an operand addresses.
+int64_t span_elems(int64_t rows, int64_t cols, int64_t ld, bool trans, int64_t batch,
+                   int64_t bstride);
+inline int64_t span_a(const Problem &p) { return span_elems(p.M, p.K, p.lda, p.at, p.batch, p.sA); }
+inline int64_t span_b(const Problem &p) { return span_elems(p.K, p.N, p.ldb, p.bt, p.batch, p.sB); }
+inline int64_t span_c(const Problem &p) { return span_elems(p.M, p.N, p.ldc, false, p.batch, p.sC); }
+
+// Fill a Problem from C-ABI arguments and check it; MM_OK or INVALID_ARG.
+mm_status make_problem(Problem *p, const void *lhs, const void *rhs, void *out, int64_t M,
+                       int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc, mm_dtypes dt,
+                       mm_layout layout, const mm_batch *batch);
+
+// ---------------------------------------------------------------- errors
+mm_status set_error(mm_status s, const char *fmt, ...);
+mm_status cuda_error(cudaError_t e, const char *what);
+#define MM_CUDA_TRY(expr)                                     \
+  do {                                                        \
+    cudaError_t e__ = (expr);                                 \
+    if (e__ != cudaSuccess) return ::mm::cuda_error(e__, #expr); \
+  } while (0)
+
+// ---------------------------------------------------------------- key
+// 64-byte plain key; every byte is defined (zero padding) so memcmp works.
+struct KeyPod {
+  uint64_t m, n, k, batch;
+  uint8_t lhs_pow2, lhs_stride, rhs_pow2, rhs_stride;
+  uint8_t elem_lhs, elem_rhs, elem_out;
+  uint8_t layout_lhs, layout_rhs;  // Layout enum
+  uint8_t scale, kind;
+  uint8_t pad[21];
+};
+static_assert(sizeof(KeyPod) == 64, "key must be 64 bytes");
+
+enum Layout : uint8_t {
+  LAYOUT_CONTIGUOUS = 0,
+  LAYOUT_MP_T = 1,    // MildlyPermuted{transposed:true,  batch_swap:false}
+  LAYOUT_MP_B = 2,    // MildlyPermuted{transposed:false, batch_swap:true}
+  LAYOUT_MP_TB = 3,   // MildlyPermuted{transposed:true,  batch_swap:true}
+  LAYOUT_HIGHLY = 4,  // HighlyPermuted (not expressible through this ABI)
+};
+enum Scale : uint8_t { SCALE_SMALL = 0, SCALE_MEDIUM = 1, SCALE_LARGE = 2 };
+enum Kind : uint8_t {
+  KIND_GENERAL = 0, KIND_MATVEC, KIND_VECMAT, KIND_SCALARVEC, KIND_VECSCALAR,
+  KIND_INNER, KIND_OUTER
+};
+enum Level { LEVEL_MINIMAL = 0, LEVEL_BALANCED = 1, LEVEL_EXTENSIVE = 2, LEVEL_FULL = 3 };
+
+uint64_t anchor(uint64_t x, int level);
+KeyPod make_key(const Problem &p, int level);
+std::string key_text(const KeyPod &k);
+bool parse_key_text(const std::string &s, KeyPod *out);
+
+struct KeyHash {
+  size_t operator()(const KeyPod &k) const;
+};
+struct KeyEq {
+  bool operator()(const KeyPod &a, const KeyPod &b) const {
+    return std::memcmp(&a, &b, sizeof(KeyPod)) == 0;
+  }
+};
+
+// ---------------------------------------------------------------- options
+struct Options {
+  int tuning = 1;
+  int autotune_cache = 1;
+  int level = LEVEL_BALANCED;
+  int max_tuning_iterations = 100;
+  double max_tuning_duration_ms = 30.0;
+  double rotating_buffer_mb = -1.0;
+  int l2_flush = 0;
+  std::string numerical_check;  // "" or "atol_rtol"
+  std::string cache_file;
+  std::string decisions;
+  int verbose = 0;
+  double peak_tflops = 0.0;
+  double peak_gbs = 0.0;
+  std::string fault;
+};
+// Snapshot of the current options (env values take precedence over the API).
+Options get_options();
+mm_status set_option(const std::string &name, const std::string &value);
+mm_status get_option(const std::string &name, std::string *value);
+
+// ---------------------------------------------------------------- device
+struct DeviceInfo {
+  int ordinal = -1;
+  int sms = 0;
+  int cc_major = 0, cc_minor = 0;
+  int64_t l2_bytes = 0;
+  int64_t smem_optin = 0;
+  int64_t total_mem = 0;
+  std::string name, uuid;
+};
+
+// Library-owned device buffer that grows on demand.
+struct DevBuf {
+  void *ptr = nullptr;
+  size_t bytes = 0;
+  mm_status ensure(size_t need);
+  void release();
+};
+
+struct TableEntry {
+  int winner = 0;               // candidate index
+  std::vector<int> ranking;     // valid candidates, fastest first
+  double median_ms = 0.0;
+  std::string detail;           // "name:median;..." for the result file
+  bool from_file = false;
+};
+
+struct Peaks {
+  bool ready = false;
+  double bf16_ops = 0, tf32_ops = 0, bytes_per_s = 0, launch_ns = 0;
+  std::string source;
+};
+
+struct DeviceState {
+  DeviceInfo info;
+  int *d_err = nullptr;                  // kernel error word (bounded-wait timeouts)
+  cudaStream_t tune_stream = nullptr;
+  cudaEvent_t ev_order = nullptr;
+  std::mutex scratch_mu;
+  // per-(stream, slot) scratch: slot SCRATCH_TICKETS holds zero-initialised
+  // counters that kernels leave at zero; SCRATCH_WORKSPACE holds partial sums
+  std::map<std::pair<cudaStream_t, int>, DevBuf> scratch;
+  DevBuf flush_buf;
+  DevBuf stage_a, stage_b, stage_c;        // host-buffer entry point staging
+  std::mutex stage_mu;
+  // tuning table
+  std::shared_mutex table_mu;
+  std::unordered_map<KeyPod, TableEntry, KeyHash, KeyEq> table;
+  std::mutex pending_mu;
+  std::condition_variable pending_cv;
+  std::unordered_set<KeyPod, KeyHash, KeyEq> pending;
+  bool file_loaded = false;
+  bool dirty = false;
+  std::mutex tune_mu;  // one tuning run at a time per device
+  Peaks peaks;
+};
+
+// The state of the current device (creating it on first use).
+mm_status current_device(DeviceState **out);
+// Drop every device state (mm_shutdown).
+void release_all_devices();
+void for_each_device(void (*fn)(DeviceState &));
+
+// Scratch of at least `bytes` private to (device, stream, slot).  A new or
+// grown buffer is zero-filled (stream-ordered).
+enum ScratchSlot { SCRATCH_TICKETS = 0, SCRATCH_WORKSPACE = 1 };
+mm_status get_scratch(DeviceState &ds, cudaStream_t s, int slot, size_t bytes, void **out);
+
+// ---------------------------------------------------------------- candidates
+enum Group { GROUP_GEMV = 0, GROUP_TENSOR = 1, GROUP_NAIVE = 2, GROUP_COUNT = 3 };
+constexpr int PRIORITY_MAX = 3, PRIORITY_HIGH = 2, PRIORITY_MEDIUM = 1, PRIORITY_MIN = 0,
+              PRIORITY_NEVER = -1;
+
+struct LaunchCtx {
+  cudaStream_t stream;
+  DeviceState *dev;
+  bool tuning;  // benchmark launch (counted separately)
+};
+
+struct Candidate {
+  std::string name;
+  int group;
+  int cfg;  // index into the family's config table
+  int (*prio)(const KeyPod &, const Problem &, const DeviceInfo &, int cfg);
+  bool (*supports)(const Problem &, const DeviceInfo &, int cfg, std::string *why);
+  mm_status (*launch)(const Problem &, LaunchCtx &, int cfg);
+};
+
+const std::vector<Candidate> &registry();
+uint64_t registry_checksum();
+int group_priority(int group, const KeyPod &k, const Problem &p, const DeviceInfo &d);
+const char *group_name(int group);
+void count_launch(int index, bool tuning);
+uint64_t candidate_launches(int index);
+
+// Plan entry: (candidate, group, tier rank, supported, group prio, prio).
+struct PlanItem {
+  int cand, group, tier, supported, group_prio, prio;
+};
+std::vector<PlanItem> make_plan(const KeyPod &k, const Problem &p, const DeviceInfo &d);
+
+// Launch one candidate with fault injection and counting applied.
+mm_status launch_candidate(int index, const Problem &p, LaunchCtx &ctx);
+
+// ---------------------------------------------------------------- kernels
+mm_status launch_naive(const Problem &p, cudaStream_t s);
+mm_status launch_l2_flush(void *buf, size_t bytes, cudaStream_t s);
+mm_status launch_empty(cudaStream_t s);
+mm_status launch_copy_probe(const void *src, void *dst, size_t bytes, cudaStream_t s);
+mm_status launch_compare(const void *x, const void *ref, int dtype, int64_t rows, int64_t cols,
+                         int64_t ld, int64_t batch, int64_t bstride, double atol, double rtol,
+                         int *d_bad, cudaStream_t s);
+
+bool gemv_supports(const Problem &p, const DeviceInfo &d, int cfg, std::string *why);
+mm_status launch_gemv(const Problem &p, LaunchCtx &ctx, int cfg);
+int gemv_config_count();
+const char *gemv_config_name(int cfg);
+
+bool tc_supports(const Problem &p, const DeviceInfo &d, int cfg, std::string *why);
+mm_status launch_tc(const Problem &p, LaunchCtx &ctx, int cfg);
+int tc_config_count();
+const char *tc_config_name(int cfg);
+bool tc_config_is_splitk(int cfg);
+
+// ---------------------------------------------------------------- tuner
+struct ExecResult {
+  int candidate = -1;
+  bool hit = false;
+};
+mm_status autotune_execute(const Problem &p, cudaStream_t s, ExecResult *res);
+mm_status roofline_peaks(DeviceState &ds, Peaks *out);
+
+// ---------------------------------------------------------------- cache file
+mm_status cache_load(DeviceState &ds, const std::string &path);
+mm_status cache_save(DeviceState &ds, const std::string &path);
+std::string device_file_name(const std::string &path, int ordinal);
+
+// ---------------------------------------------------------------- stats
+struct StatsAtomic {
+  std::atomic<uint64_t> calls{0}, hits{0}, misses{0}, tunes{0}, launches{0}, bench_launches{0};
+  std::atomic<double> last_tune_ms{0.0}, total_tune_ms{0.0};
+};
+StatsAtomic &stats();
+
+}  // namespace mm

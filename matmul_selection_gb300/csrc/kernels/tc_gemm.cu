@@ -1,0 +1,743 @@
+// Tensor-core GEMM family for sm_103a: tcgen05.mma into TMEM, fed by TMA.
+//
+// The autotune page's "accelerated" group (cooperative-matrix kernels) and its
+// TMA-fed variants are rebuilt here for Blackwell's 5th-generation tensor
+// cores.  One kernel template covers every configuration:
+//
+//   * persistent: one CTA per SM walks the work units (output tile x batch x
+//     K split) with a grid stride;
+//   * warp-specialised, 6 warps: warp 0 issues TMA loads (one elected lane),
+//     warp 1 allocates TMEM and issues tcgen05.mma (one lane), warps 2..5
+//     drain accumulators from TMEM (tcgen05.ld) and store them;
+//   * an S-stage shared-memory ring guarded by mbarriers (full: TMA bytes
+//     landed; empty: the MMAs reading the stage completed, signalled by
+//     tcgen05.commit), and two TMEM accumulators so the epilogue of one tile
+//     overlaps the main loop of the next;
+//   * tiles are 128 x BN x (128 bytes of K) with the 128-byte swizzle; A and B
+//     may each be K-major or MN-major (MN-major only for 16-bit types), so
+//     transposed views are read in place;
+//   * kind::f16 for bf16/f16 inputs, kind::tf32 for f32 inputs (f32 is
+//     multiplied as tf32: the burn backend page notes the kernel may run f32
+//     as tf32), fp32 accumulation always;
+//   * split-K configurations write fp32 partials of each K slice to a
+//     workspace; a second kernel adds the slices in increasing slice order
+//     (deterministic) and converts.  Split-K regroups additions only (the
+//     CMU 15-779 lecture's rfactor / split-K discussion);
+//   * every mbarrier wait is bounded (%globaltimer); on expiry the kernel
+//     records an error code, tells the other roles to stop, waits for its own
+//     MMAs, frees TMEM and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <mutex>
+
+#include "../common.h"
+
+namespace mm {
+
+namespace {
+
+constexpr int BM = 128;
+constexpr int kTcThreads = 192;
+constexpr uint64_t kWaitTimeoutNs = 2000000000ull;  // 2 s per wait
+
+// error codes (first one wins): 0x100 | role
+constexpr int kErrProducer = 0x101, kErrMma = 0x102, kErrEpilogue = 0x103, kErrDrain = 0x104;
+
+struct TcParams {
+  int M, N, K, batch;
+  int tiles_m, tiles_n, splits, kb_per_split, num_kb, total_units;
+  void *C;
+  int64_t ldc, sC;
+  int tc;
+  int c_vec_ok;
+  float *ws;
+  int *err;
+  uint32_t idesc;
+  uint64_t a_desc, b_desc;           // descriptor bits except the start address
+  uint32_t a_kstep, b_kstep;         // start-address advance per MMA k-step (16-byte units)
+  uint32_t a_box_stride, b_box_stride;  // bytes between the TMA boxes of one stage (MN-major)
+  int a_boxes, b_boxes, a_mn, b_mn;
+  uint64_t timeout_ns;
+};
+
+// ---------------------------------------------------------------- PTX wrappers
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Wait for the phase of `parity` to complete.  Gives up (false) when the
+// shared abort flag is raised or after timeout_ns, raising the flag and
+// recording `code` in the error word.
+__device__ __noinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                          int *err, int code, uint64_t timeout_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 32; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (global_ns() - t0 > timeout_ns) {
+      *abort_flag = 1;
+      atomicCAS(err, 0, code);
+      return false;
+    }
+  }
+}
+
+// Bounded wait that ignores the abort flag: used at the end to let copies and
+// MMAs already in flight finish before shared memory and TMEM are released.
+__device__ __noinline__ void wait_drain(uint32_t bar, uint32_t parity, int *err, int code,
+                                        uint64_t timeout_ns) {
+  const uint64_t t0 = global_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (global_ns() - t0 > timeout_ns) {
+      atomicCAS(err, 0, code);
+      return;
+    }
+  }
+}
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, uint32_t bar,
+                                            int c0, int c1, int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tmap(const CUtensorMap *map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+
+template <int ES>
+__device__ __forceinline__ void umma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                     uint32_t idesc, uint32_t accumulate) {
+  if constexpr (ES == 2) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+  } else {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+  }
+}
+
+// Arrive on `bar` once every previously issued tcgen05 op of this thread is done.
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   bar)
+               : "memory");
+}
+
+// 32 lanes x 32 consecutive 32-bit columns: thread i gets row (lane) i.
+__device__ __forceinline__ void tmem_ld_32cols(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_ld_wait() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// ---------------------------------------------------------------- epilogue store
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t *>(&v);
+}
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+  __half2 v = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t *>(&v);
+}
+
+__device__ __forceinline__ void store_chunk(const TcParams &p, int b, int sp, int row, int col0,
+                                            const uint32_t (&r)[32]) {
+  if (row >= p.M) return;
+  const bool full = col0 + 32 <= p.N;
+  if (p.splits > 1) {
+    float *dst = p.ws + (((int64_t)sp * p.batch + b) * p.M + row) * (int64_t)p.N + col0;
+    if (full && (p.N & 3) == 0) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        reinterpret_cast<float4 *>(dst)[i] =
+            make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
+                        __uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3]));
+    } else {
+      for (int i = 0; i < 32; ++i)
+        if (col0 + i < p.N) dst[i] = __uint_as_float(r[i]);
+    }
+    return;
+  }
+  const int64_t off = (int64_t)b * p.sC + (int64_t)row * p.ldc + col0;
+  if (p.tc == MM_F32) {
+    float *dst = static_cast<float *>(p.C) + off;
+    if (full && p.c_vec_ok) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        reinterpret_cast<float4 *>(dst)[i] =
+            make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
+                        __uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3]));
+    } else {
+      for (int i = 0; i < 32; ++i)
+        if (col0 + i < p.N) dst[i] = __uint_as_float(r[i]);
+    }
+  } else {
+    uint16_t *dst = static_cast<uint16_t *>(p.C) + off;
+    const bool bf = p.tc == MM_BF16;
+    if (full && p.c_vec_ok) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        uint32_t w[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          float lo = __uint_as_float(r[8 * i + 2 * j]), hi = __uint_as_float(r[8 * i + 2 * j + 1]);
+          w[j] = bf ? pack_bf16(lo, hi) : pack_f16(lo, hi);
+        }
+        reinterpret_cast<uint4 *>(dst)[i] = make_uint4(w[0], w[1], w[2], w[3]);
+      }
+    } else {
+      for (int i = 0; i < 32; ++i)
+        if (col0 + i < p.N) {
+          float v = __uint_as_float(r[i]);
+          if (bf) {
+            __nv_bfloat16 h = __float2bfloat16_rn(v);
+            dst[i] = *reinterpret_cast<uint16_t *>(&h);
+          } else {
+            __half h = __float2half_rn(v);
+            dst[i] = *reinterpret_cast<uint16_t *>(&h);
+          }
+        }
+    }
+  }
+}
+
+__device__ __forceinline__ void decode_unit(const TcParams &p, int u, int &tm, int &tn, int &b,
+                                            int &sp) {
+  sp = u % p.splits;
+  u /= p.splits;
+  tm = u % p.tiles_m;
+  u /= p.tiles_m;
+  tn = u % p.tiles_n;
+  b = u / p.tiles_n;
+}
+
+// ---------------------------------------------------------------- the kernel
+template <int BN, int STAGES, int ES>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const TcParams p) {
+  constexpr uint32_t A_BYTES = BM * 128;
+  constexpr uint32_t B_BYTES = BN * 128;
+  constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+  constexpr int BK = 128 / ES;      // K elements per stage (one 128-byte swizzle row)
+  constexpr int UMMA_K = 32 / ES;   // K per tcgen05.mma (32 bytes)
+  constexpr int KSTEPS = BK / UMMA_K;
+  constexpr uint32_t TMEM_COLS = 2 * BN;
+  constexpr int ATOM = 128 / ES;    // elements per 128-byte row (MN-major box width)
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                              ~static_cast<uintptr_t>(1023));
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + STAGES * STAGE_BYTES);
+  const uint32_t full0 = smem_u32(bars);
+  const uint32_t empty0 = full0 + 8 * STAGES;
+  const uint32_t tfull0 = empty0 + 8 * STAGES;
+  const uint32_t tempty0 = tfull0 + 16;
+  const uint32_t drain = tempty0 + 16;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * STAGES + 5);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(tfull0 + 8 * a, 1);
+      mbar_init(tempty0 + 8 * a, 4);  // one arrival per epilogue warp
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < p.total_units && ok; u += gridDim.x) {
+        int tm, tn, b, sp;
+        decode_unit(p, u, tm, tn, b, sp);
+        const int kb0 = sp * p.kb_per_split;
+        const int kb1 = min(p.num_kb, kb0 + p.kb_per_split);
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (!wait_bounded(empty0 + 8 * stage, phase ^ 1, abort_flag, p.err, kErrProducer,
+                            p.timeout_ns)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = full0 + 8 * stage;
+          const uint32_t sa = smem_u32(smem + stage * STAGE_BYTES);
+          const uint32_t sb = sa + A_BYTES;
+          mbar_expect_tx(fb, STAGE_BYTES);
+          if (!p.a_mn) {
+            tma_load_3d(sa, &tmA, fb, kb * BK, tm * BM, b);
+          } else {
+            for (int j = 0; j < p.a_boxes; ++j)
+              tma_load_3d(sa + j * p.a_box_stride, &tmA, fb, tm * BM + j * ATOM, kb * BK, b);
+          }
+          if (!p.b_mn) {
+            tma_load_3d(sb, &tmB, fb, kb * BK, tn * BN, b);
+          } else {
+            for (int j = 0; j < p.b_boxes; ++j)
+              tma_load_3d(sb + j * p.b_box_stride, &tmB, fb, tn * BN + j * ATOM, kb * BK, b);
+          }
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      // Leave no copy in flight: wait until the MMA warp has released every
+      // stage we filled (normal path), or at least until our last fills
+      // landed (abort path).
+      for (int s = 0; s < STAGES; ++s) {
+        // the most recent fill of `stage` (walking backwards) used parity:
+        int st = (stage + s) % STAGES;
+        uint32_t par = (st < stage) ? phase : phase ^ 1;  // last completed-or-pending fill
+        wait_drain(full0 + 8 * st, par, p.err, kErrProducer, p.timeout_ns);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < p.total_units && ok; u += gridDim.x) {
+        int tm, tn, b, sp;
+        decode_unit(p, u, tm, tn, b, sp);
+        const int kb0 = sp * p.kb_per_split;
+        const int kb1 = min(p.num_kb, kb0 + p.kb_per_split);
+        if (!wait_bounded(tempty0 + 8 * acc, acc_phase ^ 1, abort_flag, p.err, kErrMma,
+                          p.timeout_ns))
+          break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (!wait_bounded(full0 + 8 * stage, phase, abort_flag, p.err, kErrMma, p.timeout_ns)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(smem + stage * STAGE_BYTES);
+          const uint32_t sb = sa + A_BYTES;
+          const uint64_t adesc = p.a_desc | (uint64_t)((sa >> 4) & 0x3FFFu);
+          const uint64_t bdesc = p.b_desc | (uint64_t)((sb >> 4) & 0x3FFFu);
+#pragma unroll
+          for (int kk = 0; kk < KSTEPS; ++kk)
+            umma<ES>(d_tmem, adesc + (uint64_t)(kk * p.a_kstep), bdesc + (uint64_t)(kk * p.b_kstep),
+                     p.idesc, (kb > kb0 || kk > 0) ? 1u : 0u);
+          umma_commit(empty0 + 8 * stage);  // frees the stage when these MMAs finish
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (!ok) break;
+        umma_commit(tfull0 + 8 * acc);  // accumulator ready for the epilogue
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1;
+        }
+      }
+      // every MMA this thread issued is complete before TMEM is released
+      umma_commit(drain);
+      wait_drain(drain, 0, p.err, kErrDrain, p.timeout_ns);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int u = blockIdx.x; u < p.total_units; u += gridDim.x) {
+      int tm, tn, b, sp;
+      decode_unit(p, u, tm, tn, b, sp);
+      int ok = 1;
+      if (lane == 0)
+        ok = wait_bounded(tfull0 + 8 * acc, acc_phase, abort_flag, p.err, kErrEpilogue,
+                          p.timeout_ns);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      tc_fence_after();
+      const int row = tm * BM + q * 32 + lane;
+      const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld_32cols(tbase + (uint32_t)(c * 32), r);
+        tmem_ld_wait();
+        store_chunk(p, b, sp, row, tn * BN + c * 32, r);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty0 + 8 * acc);
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1;
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem_base, TMEM_COLS);
+}
+
+// Sum the split-K partials in increasing slice order and convert.
+__global__ void splitk_reduce_kernel(const float *__restrict__ ws, int S, int batch, int M, int N,
+                                     void *C, int tc, int64_t ldc, int64_t sC) {
+  const int64_t MN = (int64_t)M * N;
+  const int64_t total = (int64_t)batch * MN;
+  const int64_t SBMN = (int64_t)batch * MN;
+  for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total;
+       e += (int64_t)gridDim.x * blockDim.x) {
+    float sum = 0.f;
+    for (int s = 0; s < S; ++s) sum += __ldcs(ws + s * SBMN + e);
+    const int64_t b = e / MN, rem = e - b * MN, i = rem / N, j = rem - i * N;
+    const int64_t off = b * sC + i * ldc + j;
+    if (tc == MM_F32)
+      static_cast<float *>(C)[off] = sum;
+    else if (tc == MM_BF16)
+      static_cast<__nv_bfloat16 *>(C)[off] = __float2bfloat16_rn(sum);
+    else
+      static_cast<__half *>(C)[off] = __float2half_rn(sum);
+  }
+}
+
+// ---------------------------------------------------------------- host side
+struct TcCfg {
+  const char *name;
+  int bn;
+  int stages;
+  bool splitk;
+};
+
+const TcCfg kCfgs[] = {
+    {"tc_128x256_s4", 256, 4, false},
+    {"tc_128x128_s6", 128, 6, false},
+    {"tc_128x64_s8", 64, 8, false},
+    {"tc_splitk_128x128_s6", 128, 6, true},
+    {"tc_splitk_128x64_s8", 64, 8, true},
+};
+
+size_t smem_bytes(int bn, int stages) {
+  return (size_t)stages * (BM * 128 + bn * 128) + 1024 + 256;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+CUtensorMapDataType map_dtype(int t) {
+  return t == MM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+         : t == MM_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                       : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+}
+
+// 3-D tiled map over (inner, outer, batch) with the 128-byte swizzle.
+mm_status encode_map(CUtensorMap *map, int dtype, const void *base, uint64_t inner, uint64_t outer,
+                     uint64_t batch, uint64_t ld_bytes, uint64_t bstride_bytes, uint32_t box_inner,
+                     uint32_t box_outer) {
+  auto fn = encode_fn();
+  if (!fn) return set_error(MM_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
+  cuuint64_t dims[3] = {inner, outer, batch};
+  if (batch <= 1) bstride_bytes = ((ld_bytes * outer) + 15) & ~(uint64_t)15;
+  cuuint64_t strides[2] = {ld_bytes, bstride_bytes};
+  cuuint32_t box[3] = {box_inner, box_outer, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, map_dtype(dtype), 3, const_cast<void *>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return set_error(MM_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  return MM_OK;
+}
+
+uint64_t smem_desc_bits(uint32_t lbo_bytes, uint32_t sbo_bytes) {
+  uint64_t d = 0;
+  d |= (uint64_t)((lbo_bytes >> 4) & 0x3FFFu) << 16;  // leading-dimension byte offset
+  d |= (uint64_t)((sbo_bytes >> 4) & 0x3FFFu) << 32;  // stride-dimension byte offset
+  d |= (uint64_t)1 << 46;                             // descriptor version (tcgen05)
+  d |= (uint64_t)2 << 61;                             // 128-byte swizzle
+  return d;
+}
+
+template <int BN, int STAGES, int ES>
+mm_status launch_kernel(const CUtensorMap &ma, const CUtensorMap &mb, const TcParams &tp, int grid,
+                        cudaStream_t s) {
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  const size_t smem = smem_bytes(BN, STAGES);
+  std::call_once(once, [&] {
+    attr_err = cudaFuncSetAttribute(tc_gemm_kernel<BN, STAGES, ES>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  });
+  if (attr_err != cudaSuccess) return cuda_error(attr_err, "cudaFuncSetAttribute (tc smem)");
+  tc_gemm_kernel<BN, STAGES, ES><<<grid, kTcThreads, smem, s>>>(ma, mb, tp);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_error(e, "tc_gemm_kernel launch");
+  return MM_OK;
+}
+
+template <int ES>
+mm_status dispatch(int cfg, const CUtensorMap &ma, const CUtensorMap &mb, const TcParams &tp,
+                   int grid, cudaStream_t s) {
+  switch (kCfgs[cfg].bn) {
+  case 256: return launch_kernel<256, 4, ES>(ma, mb, tp, grid, s);
+  case 128: return launch_kernel<128, 6, ES>(ma, mb, tp, grid, s);
+  default: return launch_kernel<64, 8, ES>(ma, mb, tp, grid, s);
+  }
+}
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Split count for a split-K configuration: enough units to fill the SMs.
+void choose_splits(int64_t tiles, int64_t num_kb, int sms, int *splits, int *kb_per) {
+  int64_t s = sms / (tiles > 0 ? tiles : 1);
+  if (s < 2) s = 2;
+  if (s > num_kb) s = num_kb;
+  int64_t per = ceil_div(num_kb, s);
+  *kb_per = (int)per;
+  *splits = (int)ceil_div(num_kb, per);
+}
+
+}  // namespace
+
+int tc_config_count() { return (int)(sizeof kCfgs / sizeof kCfgs[0]); }
+const char *tc_config_name(int cfg) { return kCfgs[cfg].name; }
+bool tc_config_is_splitk(int cfg) { return kCfgs[cfg].splitk; }
+
+bool tc_supports(const Problem &p, const DeviceInfo &d, int cfg, std::string *why) {
+  auto no = [&](const char *w) {
+    if (why) *why = w;
+    return false;
+  };
+  const TcCfg &c = kCfgs[cfg];
+  if (d.cc_major != 10 || d.cc_minor != 3) return no("needs an sm_103 device");
+  if (p.ta != p.tb) return no("A and B must have the same type");
+  if (p.M < 1 || p.N < 1 || p.K < 1) return no("empty problem");
+  if (p.M >= (1LL << 31) || p.N >= (1LL << 31) || p.K >= (1LL << 31) || p.batch >= (1LL << 31))
+    return no("dimension too large");
+  const int es = dtype_bytes(p.ta);
+  if (es == 4 && (p.at || !p.bt)) return no("f32 (tf32) needs K-major A and B (layout NT)");
+  if ((uintptr_t)p.A % 16 || (uintptr_t)p.B % 16) return no("A or B not 16-byte aligned");
+  if ((p.lda * es) % 16 || (p.ldb * es) % 16)
+    return no("lda/ldb not a multiple of 16 bytes (TMA stride rule)");
+  if (p.batch > 1) {
+    if (p.sA <= 0 || p.sB <= 0) return no("zero batch stride");
+    if ((p.sA * es) % 16 || (p.sB * es) % 16) return no("batch stride not a multiple of 16 bytes");
+  }
+  if (p.lda * es >= (1LL << 40) || p.ldb * es >= (1LL << 40) || p.sA * es >= (1LL << 40) ||
+      p.sB * es >= (1LL << 40))
+    return no("stride too large for TMA");
+  if ((int64_t)smem_bytes(c.bn, c.stages) > d.smem_optin) return no("not enough shared memory");
+  if (c.splitk) {
+    const int64_t num_kb = ceil_div(p.K, 128 / es);
+    if (num_kb < 2) return no("split-K needs at least two K blocks");
+  }
+  return true;
+}
+
+mm_status launch_tc(const Problem &p, LaunchCtx &ctx, int cfg) {
+  std::string why;
+  if (!tc_supports(p, ctx.dev->info, cfg, &why))
+    return set_error(MM_ERR_UNSUPPORTED, "%s: %s", kCfgs[cfg].name, why.c_str());
+  const TcCfg &c = kCfgs[cfg];
+  const int es = dtype_bytes(p.ta);
+  const int bk = 128 / es, atom = 128 / es, umma_k = 32 / es;
+  const int bn = c.bn;
+  CUtensorMap ma, mb;
+  mm_status st;
+  // A: logical M x K.  K-major when stored row-major (N), MN-major when T.
+  if (!p.at)
+    st = encode_map(&ma, p.ta, p.A, p.K, p.M, p.batch, p.lda * es, p.sA * es, bk, BM);
+  else
+    st = encode_map(&ma, p.ta, p.A, p.M, p.K, p.batch, p.lda * es, p.sA * es, atom, bk);
+  if (st != MM_OK) return st;
+  // B: logical K x N.  K-major when stored transposed (T), MN-major when N.
+  if (p.bt)
+    st = encode_map(&mb, p.tb, p.B, p.K, p.N, p.batch, p.ldb * es, p.sB * es, bk, bn);
+  else
+    st = encode_map(&mb, p.tb, p.B, p.N, p.K, p.batch, p.ldb * es, p.sB * es, atom, bk);
+  if (st != MM_OK) return st;
+
+  TcParams tp;
+  std::memset(&tp, 0, sizeof tp);
+  tp.M = (int)p.M;
+  tp.N = (int)p.N;
+  tp.K = (int)p.K;
+  tp.batch = (int)p.batch;
+  tp.tiles_m = (int)ceil_div(p.M, BM);
+  tp.tiles_n = (int)ceil_div(p.N, bn);
+  tp.num_kb = (int)ceil_div(p.K, bk);
+  const int64_t tiles = (int64_t)tp.tiles_m * tp.tiles_n * tp.batch;
+  if (c.splitk) {
+    choose_splits(tiles, tp.num_kb, ctx.dev->info.sms, &tp.splits, &tp.kb_per_split);
+  } else {
+    tp.splits = 1;
+    tp.kb_per_split = tp.num_kb;
+  }
+  const int64_t units = tiles * tp.splits;
+  if (units >= (1LL << 31)) return set_error(MM_ERR_UNSUPPORTED, "too many work units");
+  tp.total_units = (int)units;
+  tp.C = p.C;
+  tp.ldc = p.ldc;
+  tp.sC = p.sC;
+  tp.tc = p.tc;
+  const int ec = dtype_bytes(p.tc);
+  tp.c_vec_ok = ((uintptr_t)p.C % 16 == 0) && ((p.ldc * ec) % 16 == 0) &&
+                (p.batch <= 1 || (p.sC * ec) % 16 == 0);
+  tp.err = ctx.dev->d_err;
+  tp.timeout_ns = kWaitTimeoutNs;
+  tp.a_mn = p.at ? 1 : 0;
+  tp.b_mn = p.bt ? 0 : 1;
+  const uint32_t fmt = p.ta == MM_F16 ? 0u : p.ta == MM_BF16 ? 1u : 2u;
+  tp.idesc = (1u << 4)                        // D: f32
+             | (fmt << 7) | (fmt << 10)       // A, B types
+             | ((uint32_t)tp.a_mn << 15)      // A major (1 = MN)
+             | ((uint32_t)tp.b_mn << 16)      // B major (1 = MN)
+             | ((uint32_t)(bn >> 3) << 17)    // N / 8
+             | ((uint32_t)(BM >> 4) << 24);   // M / 16
+  // K-major: 8-row groups 1024 B apart, K advances 32 B inside the swizzle row.
+  // MN-major: boxes of 128 bytes x bk rows; atoms along MN are bk*128 B apart,
+  // 8-row K groups 1024 B apart, K advances umma_k rows (umma_k * 128 B).
+  const uint32_t mn_atom_bytes = (uint32_t)bk * 128u;
+  tp.a_desc = tp.a_mn ? smem_desc_bits(mn_atom_bytes, 1024) : smem_desc_bits(16, 1024);
+  tp.b_desc = tp.b_mn ? smem_desc_bits(mn_atom_bytes, 1024) : smem_desc_bits(16, 1024);
+  tp.a_kstep = tp.a_mn ? (uint32_t)(umma_k * 128) >> 4 : 32u >> 4;
+  tp.b_kstep = tp.b_mn ? (uint32_t)(umma_k * 128) >> 4 : 32u >> 4;
+  tp.a_boxes = tp.a_mn ? BM / atom : 1;
+  tp.b_boxes = tp.b_mn ? bn / atom : 1;
+  tp.a_box_stride = mn_atom_bytes;
+  tp.b_box_stride = mn_atom_bytes;
+  if (tp.splits > 1) {
+    void *w = nullptr;
+    size_t ws_bytes = (size_t)tp.splits * tp.batch * (size_t)p.M * p.N * sizeof(float);
+    st = get_scratch(*ctx.dev, ctx.stream, SCRATCH_WORKSPACE, ws_bytes, &w);
+    if (st != MM_OK) return st;
+    tp.ws = static_cast<float *>(w);
+  }
+  const int grid = (int)std::min<int64_t>(units, ctx.dev->info.sms);
+  st = es == 2 ? dispatch<2>(cfg, ma, mb, tp, grid, ctx.stream)
+               : dispatch<4>(cfg, ma, mb, tp, grid, ctx.stream);
+  if (st != MM_OK) return st;
+  if (tp.splits > 1) {
+    const int64_t total = (int64_t)tp.batch * p.M * p.N;
+    int blocks = (int)std::min<int64_t>(ceil_div(total, 256), (int64_t)ctx.dev->info.sms * 8);
+    splitk_reduce_kernel<<<blocks, 256, 0, ctx.stream>>>(tp.ws, tp.splits, tp.batch, tp.M, tp.N,
+                                                         p.C, p.tc, p.ldc, p.sC);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_error(e, "splitk_reduce_kernel launch");
+  }
+  return MM_OK;
+}
+
+}  // namespace mm

@@ -1,0 +1,86 @@
+// Utility kernels of the tuner: L2 flush, probes and the numerical check.
+//
+// The probes follow the burn "autotune" page, section "roofline and the
+// hundred thousand launches": an almost empty kernel whose repeated launches
+// measure the launch overhead, and a memory-copy kernel whose throughput is
+// the bandwidth peak of the roofline bound.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "../common.h"
+
+namespace mm {
+
+namespace {
+
+__global__ void empty_kernel(int *p) {
+  if (p && blockIdx.x == 0 && threadIdx.x == 0) *p = 0;
+}
+
+// Grid-stride 16-byte writes over a buffer larger than L2, evicting it.
+__global__ void flush_kernel(uint4 *buf, size_t n16, unsigned seed) {
+  size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  size_t stride = (size_t)gridDim.x * blockDim.x;
+  for (; i < n16; i += stride) buf[i] = make_uint4(seed, (unsigned)i, seed, (unsigned)i);
+}
+
+// Grid-stride 16-byte copy: the bandwidth probe.
+__global__ void copy_kernel(const uint4 *__restrict__ src, uint4 *__restrict__ dst, size_t n16) {
+  size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  size_t stride = (size_t)gridDim.x * blockDim.x;
+  for (; i < n16; i += stride) dst[i] = src[i];
+}
+
+__device__ __forceinline__ float ld_any(const void *p, int64_t i, int t) {
+  if (t == MM_F32) return static_cast<const float *>(p)[i];
+  if (t == MM_BF16) return __bfloat162float(static_cast<const __nv_bfloat16 *>(p)[i]);
+  return __half2float(static_cast<const __half *>(p)[i]);
+}
+
+// *bad |= |x - ref| > atol + rtol * |ref| over the logical outputs.
+__global__ void compare_kernel(const void *x, const void *ref, int t, int64_t rows, int64_t cols,
+                               int64_t ld, int64_t batch, int64_t bstride, float atol, float rtol,
+                               int *bad) {
+  int64_t total = rows * cols * batch;
+  for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total;
+       e += (int64_t)gridDim.x * blockDim.x) {
+    int64_t b = e / (rows * cols), r = (e / cols) % rows, c = e % cols;
+    int64_t off = b * bstride + r * ld + c;
+    float a = ld_any(x, off, t), q = ld_any(ref, off, t);
+    if (!(fabsf(a - q) <= atol + rtol * fabsf(q))) atomicOr(bad, 1);
+  }
+}
+
+}  // namespace
+
+mm_status launch_empty(cudaStream_t s) {
+  empty_kernel<<<1, 32, 0, s>>>(nullptr);
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? MM_OK : cuda_error(e, "empty_kernel launch");
+}
+
+mm_status launch_l2_flush(void *buf, size_t bytes, cudaStream_t s) {
+  static unsigned seed = 1;
+  size_t n16 = bytes / 16;
+  flush_kernel<<<1024, 256, 0, s>>>(static_cast<uint4 *>(buf), n16, seed++);
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? MM_OK : cuda_error(e, "flush_kernel launch");
+}
+
+mm_status launch_copy_probe(const void *src, void *dst, size_t bytes, cudaStream_t s) {
+  copy_kernel<<<2048, 256, 0, s>>>(static_cast<const uint4 *>(src), static_cast<uint4 *>(dst),
+                                   bytes / 16);
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? MM_OK : cuda_error(e, "copy_kernel launch");
+}
+
+mm_status launch_compare(const void *x, const void *ref, int dtype, int64_t rows, int64_t cols,
+                         int64_t ld, int64_t batch, int64_t bstride, double atol, double rtol,
+                         int *d_bad, cudaStream_t s) {
+  compare_kernel<<<1024, 256, 0, s>>>(x, ref, dtype, rows, cols, ld, batch, bstride, (float)atol,
+                                      (float)rtol, d_bad);
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? MM_OK : cuda_error(e, "compare_kernel launch");
+}
+
+}  // namespace mm

@@ -1,0 +1,167 @@
+"""Every candidate against the CPU oracle, through the C ABI (GPU).
+
+Bar (from the method's correctness target): integer-valued inputs in
+{-4..4} with K <= 4096 must match the oracle bit-exactly (every partial sum
+is an integer below 2^24, exact in fp32 in any order; the single rounding to
+the output type is round-to-nearest-even on both sides); real-valued inputs
+must reach a relative Frobenius error <= 2e-3.  Every candidate, not only the
+tuner's choice, is held to it.  Output padding must never be written.
+"""
+import numpy as np
+import pytest
+
+import matmul_selection_gb300 as mm
+import oracle
+from gpu_util import BF16, F16, F32, Case
+
+pytestmark = pytest.mark.gpu
+
+NAMES = mm.candidate_names()
+CANDS = list(range(len(NAMES)))
+LAYOUTS = ["NN", "NT", "TN", "TT"]
+
+
+def run(cand, case):
+    return mm.mm_execute_candidate(cand, *case.args())
+
+
+def _expect_supported_or_skip(st, cand, case):
+    if st == mm.MM_ERR_UNSUPPORTED:
+        return False
+    assert st == mm.MM_OK, f"{NAMES[cand]}: {mm.mm_last_error()}"
+    return True
+
+
+SMALL = [(256, 256, 256), (17, 33, 65), (3, 5, 7), (1, 1, 1), (130, 260, 200),
+         (16, 72, 1000), (8, 1000, 1001), (200, 136, 64)]
+
+
+@pytest.mark.parametrize("cand", CANDS, ids=NAMES)
+@pytest.mark.parametrize("layout", LAYOUTS)
+@pytest.mark.parametrize("shape", SMALL, ids=lambda s: "x".join(map(str, s)))
+def test_integer_exact_bf16_to_f32(cand, layout, shape):
+    c = Case(*shape, layout=layout, dt=(BF16, BF16, F32), dist="int4").device()
+    if _expect_supported_or_skip(run(cand, c), cand, c):
+        c.check(exact=True)
+
+
+@pytest.mark.parametrize("cand", CANDS, ids=NAMES)
+@pytest.mark.parametrize("dt", [(BF16, BF16, BF16), (F16, F16, F32), (F16, F16, F16),
+                                (F32, F32, F32), (F32, F32, BF16)],
+                         ids=["bf16-bf16", "f16-f32", "f16-f16", "f32-f32", "f32-bf16"])
+@pytest.mark.parametrize("layout", LAYOUTS)
+def test_integer_exact_dtypes(cand, dt, layout):
+    c = Case(16, 264, 520, layout=layout, dt=dt, dist="int4", seed=7).device()
+    if _expect_supported_or_skip(run(cand, c), cand, c):
+        c.check(exact=True)
+    c = Case(140, 96, 300, layout=layout, dt=dt, dist="int4", seed=8).device()
+    if _expect_supported_or_skip(run(cand, c), cand, c):
+        c.check(exact=True)
+
+
+@pytest.mark.parametrize("cand", CANDS, ids=NAMES)
+@pytest.mark.parametrize("layout", LAYOUTS)
+@pytest.mark.parametrize("dt", [(BF16, BF16, F32), (BF16, BF16, BF16), (F32, F32, F32)],
+                         ids=["bf16-f32", "bf16-bf16", "f32-f32"])
+def test_real_valued_frobenius(cand, layout, dt):
+    for shape in [(256, 256, 256), (16, 520, 777), (129, 200, 3000)]:
+        c = Case(*shape, layout=layout, dt=dt, dist="normal", seed=11).device()
+        if _expect_supported_or_skip(run(cand, c), cand, c):
+            c.check(exact=False)
+
+
+@pytest.mark.parametrize("cand", CANDS, ids=NAMES)
+def test_batched_with_gaps(cand):
+    # batch strides leave NaN-filled gaps between items; C items too
+    for layout in LAYOUTS:
+        c = Case(12, 40, 72, layout=layout, dt=(BF16, BF16, F32), dist="int4", batch=3,
+                 bstride_extra=(8, 16, 8), pad=(8, 8, 4)).device()
+        if _expect_supported_or_skip(run(cand, c), cand, c):
+            c.check(exact=True)
+
+
+@pytest.mark.parametrize("cand", CANDS, ids=NAMES)
+def test_padded_and_misaligned_lda(cand):
+    # lda = K + 4 (bf16: 8-byte aligned rows), ldc padded
+    c = Case(16, 256, 512, layout="NN", dt=(BF16, BF16, F32), dist="int4", pad=(4, 0, 3)).device()
+    if _expect_supported_or_skip(run(cand, c), cand, c):
+        c.check(exact=True)
+    # base pointers offset by 2 bytes
+    c = Case(8, 128, 96, layout="NN", dt=(BF16, BF16, F32), dist="int4", a_off=2, c_off=4).device()
+    if _expect_supported_or_skip(run(cand, c), cand, c):
+        c.check(exact=True)
+
+
+def test_every_candidate_runs_somewhere():
+    """Coverage guard: each candidate is supported on at least one home case."""
+    home = {
+        "naive": Case(33, 17, 9, dist="int4"),
+        "gemv_n": Case(4, 256, 512, layout="NN", dist="int4"),
+        "gemv_t": Case(4, 256, 512, layout="NT", dist="int4"),
+    }
+    for i, n in enumerate(NAMES):
+        c = home.get(n) or Case(256, 256, 256, layout="NN", dist="int4")
+        c.device()
+        st = run(i, c)
+        assert st == mm.MM_OK, f"{n} unsupported on its home case: {mm.mm_last_error()}"
+        c.check(exact=True)
+
+
+def test_empty_and_zero_k():
+    for i in CANDS:
+        c = Case(0, 8, 8).device()
+        assert run(i, c) in (mm.MM_OK, mm.MM_ERR_UNSUPPORTED)
+    c = Case(5, 7, 0, dt=(BF16, BF16, F32)).device()
+    assert run(0, c) == mm.MM_OK
+    got = c.result().view(np.float32)[:35]
+    assert np.all(got == 0.0)
+
+
+def test_transposed_view_worked_example():
+    """d . d^T with the rhs a transposed view of d (strides [1, 3]); one launch."""
+    import torch
+    d = torch.tensor([[21., 42., 63.], [84., 105., 126.]], device="cuda")
+    out = torch.empty(2, 2, device="cuda")
+    for i in CANDS:
+        out.fill_(float("nan"))
+        st = mm.mm_execute_candidate(i, d, d, out, 2, 2, 3, 3, 3, 2, (F32, F32, F32), "NT")
+        if st == mm.MM_ERR_UNSUPPORTED:
+            continue
+        assert st == 0, mm.mm_last_error()
+        torch.cuda.synchronize()
+        assert out.cpu().tolist() == [[6174.0, 14112.0], [14112.0, 33957.0]], NAMES[i]
+
+
+def test_results_deterministic():
+    for i in CANDS:
+        c = Case(16, 512, 2048, layout="NN", dt=(BF16, BF16, F32), dist="normal").device()
+        if run(i, c) != mm.MM_OK:
+            continue
+        r1 = c.result().copy()
+        assert run(i, c) == mm.MM_OK
+        assert np.array_equal(r1.view(np.uint8), c.result().view(np.uint8)), NAMES[i]
+
+
+# ---------------------------------------------------------------- full sizes
+@pytest.mark.parametrize("M", [1, 8, 16])
+@pytest.mark.parametrize("layout", ["NN", "NT"])
+def test_gemv_full_size_exact(M, layout):
+    """The GEMV workload at full size (N = K = 4096), every GEMV candidate."""
+    c = Case(M, 4096, 4096, layout=layout, dt=(BF16, BF16, BF16), dist="int4").device()
+    ran = 0
+    for i, n in enumerate(NAMES):
+        if not n.startswith("gemv"):
+            continue
+        if run(i, c) == mm.MM_OK:
+            c.check(exact=True)
+            ran += 1
+    assert ran == 1
+
+
+@pytest.mark.parametrize("M", [1, 8, 16])
+def test_gemv_full_size_real(M):
+    c = Case(M, 4096, 4096, layout="NN", dt=(BF16, BF16, BF16), dist="normal",
+             dist_b="normal:0.02").device()
+    i = NAMES.index("gemv_n")
+    assert run(i, c) == mm.MM_OK
+    c.check(exact=False)

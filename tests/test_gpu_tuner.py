@@ -1,0 +1,326 @@
+"""The tuner through the C ABI (GPU): table hits and misses, the result file
+and its validators, the plan, host-side fault injection, the numerical
+check, the decision log and the host-buffer entry point."""
+import json
+import os
+import threading
+
+import numpy as np
+import pytest
+
+import matmul_selection_gb300 as mm
+import oracle
+import synth
+from gpu_util import BF16, F32, Case, logical_out, padding_untouched
+from oracle import plan as oplan
+
+pytestmark = pytest.mark.gpu
+
+NAMES = mm.candidate_names()
+DEFAULTS = {"tuning": "1", "autotune_cache": "1", "fault": "", "numerical_check": "",
+            "decisions": "", "cache_file": "", "max_tuning_iterations": "100",
+            "max_tuning_duration_ms": "30", "l2_flush": "0", "rotating_buffer_mb": "-1"}
+
+
+@pytest.fixture(autouse=True)
+def fresh_table():
+    import torch
+    torch.cuda.init()
+    for k, v in DEFAULTS.items():
+        mm.check(mm.mm_set_option(k, v))
+    mm.check(mm.mm_cache_clear())
+    mm.mm_reset_stats()
+    yield
+    for k, v in DEFAULTS.items():
+        mm.mm_set_option(k, v)
+    mm.mm_cache_clear()
+
+
+def execute(c):
+    return mm.mm_autotune_execute(*c.args())
+
+
+def test_tune_then_hit_one_launch():
+    c = Case(256, 256, 256, dist="int4").device()
+    mm.check(execute(c))
+    c.check(exact=True)
+    s = mm.mm_get_stats()
+    assert s["misses"] == 1 and s["tunes"] == 1 and s["hits"] == 0
+    launches = s["launches"]
+    for _ in range(5):
+        mm.check(execute(c))
+    c.check(exact=True)
+    s = mm.mm_get_stats()
+    assert s["hits"] == 5
+    assert s["launches"] == launches + 5  # a warm call is exactly one launch
+
+
+def test_bucket_sharing_story():
+    """f32 squares 1024, 768, 1000, 2048 in one process: 768 reuses 1024's
+    entry (one launch), 1000 has stride factor 5 and re-tunes, the table ends
+    with three entries."""
+    f32 = (F32, F32, F32)
+    for n, expect_hit in [(1024, False), (768, True), (1000, False), (2048, False)]:
+        c = Case(n, n, n, dt=f32, dist="int4", seed=n).device()
+        before = mm.mm_get_stats()
+        mm.check(execute(c))
+        after = mm.mm_get_stats()
+        assert (after["hits"] - before["hits"] == 1) == expect_hit, n
+        if expect_hit:
+            assert after["launches"] - before["launches"] == 1
+        c.check(exact=True)
+    assert mm.mm_cache_size() == 3
+
+
+def test_lookup_and_key():
+    c = Case(64, 64, 64, dist="int4").device()
+    mm.check(execute(c))
+    st, kb, _ = mm.mm_tune_key(64, 64, 64, 64, 64, 64, (BF16, BF16, F32), "NN")
+    st, idx = mm.mm_lookup(kb)
+    assert st == 0 and 0 <= idx < len(NAMES)
+    st, kb2, _ = mm.mm_tune_key(64, 64, 65, 65, 64, 64, (BF16, BF16, F32), "NN")
+    assert mm.mm_lookup(kb2) == (mm.MM_ERR_NOT_FOUND, -1)
+
+
+def test_result_file_roundtrip(tmp_path):
+    cases = [Case(256, 256, 256, dist="int4"), Case(1, 4096, 4096, dist="int4"),
+             Case(8, 512, 512, layout="NT", dist="int4")]
+    winners = {}
+    for c in cases:
+        c.device()
+        mm.check(execute(c))
+        st, kb, _ = mm.mm_tune_key(*c.args()[3:11])
+        winners[kb] = mm.mm_lookup(kb)[1]
+    path = str(tmp_path / "results.csv")
+    mm.check(mm.mm_cache_save(path))
+    lines = open(path).read().splitlines()
+    vals = {l.split(",")[1] for l in lines if l.startswith("Validator,")}
+    assert vals == {"MM_VERSION", "CANDIDATE_CHECKSUM", "DEVICE", "CUDA_VERSION"}
+    assert sum(l.startswith("MatmulKey,") for l in lines) == 3
+    mm.check(mm.mm_cache_clear())
+    assert mm.mm_cache_size() == 0
+    mm.check(mm.mm_cache_load(path))
+    assert mm.mm_cache_size() == 3
+    for kb, w in winners.items():
+        assert mm.mm_lookup(kb)[1] == w
+    # loaded entries are hits: no tuning
+    before = mm.mm_get_stats()
+    for c in cases:
+        mm.check(execute(c))
+        c.check(exact=True)
+    after = mm.mm_get_stats()
+    assert after["tunes"] == before["tunes"] and after["hits"] - before["hits"] == 3
+
+
+@pytest.mark.parametrize("field", ["MM_VERSION", "CANDIDATE_CHECKSUM", "DEVICE", "CUDA_VERSION"])
+def test_validator_mismatch_rejects_whole_file(tmp_path, field):
+    c = Case(64, 64, 64, dist="int4").device()
+    mm.check(execute(c))
+    path = str(tmp_path / "r.csv")
+    mm.check(mm.mm_cache_save(path))
+    text = open(path).read().splitlines()
+    text = [l + "x" if l.startswith(f"Validator,{field},") else l for l in text]
+    open(path, "w").write("\n".join(text) + "\n")
+    mm.check(mm.mm_cache_clear())
+    assert mm.mm_cache_load(path) == mm.MM_ERR_CACHE_VALIDATION
+    assert field in mm.mm_last_error()
+    assert mm.mm_cache_size() == 0
+
+
+def test_hand_edits_default_and_unknown_name(tmp_path):
+    ca = Case(64, 64, 64, dist="int4").device()
+    cb = Case(128, 64, 64, dist="int4").device()
+    mm.check(execute(ca))
+    mm.check(execute(cb))
+    path = str(tmp_path / "r.csv")
+    mm.check(mm.mm_cache_save(path))
+    lines = open(path).read().splitlines()
+    keys = [l for l in lines if l.startswith("MatmulKey,")]
+    out = []
+    for l in lines:
+        if l == keys[0]:
+            f = l.split(",")
+            f[2] = "Default"
+            f = f[:4]
+            l = ",".join(f)
+        elif l == keys[1]:
+            f = l.split(",")
+            f[2] = "no_such_kernel"
+            l = ",".join(f)
+        out.append(l)
+    open(path, "w").write("\n".join(out) + "\n")
+    mm.check(mm.mm_cache_clear())
+    mm.check(mm.mm_cache_load(path))
+    assert mm.mm_cache_size() == 1  # the unknown-name row was skipped
+    k0 = keys[0].split(",")[1]
+    st, kb, _ = mm.mm_tune_key(64, 64, 64, 64, 64, 64, (BF16, BF16, F32), "NN")
+    which = mm.mm_lookup(kb)[1]
+    st, kb2, _ = mm.mm_tune_key(128, 64, 64, 64, 64, 64, (BF16, BF16, F32), "NN")
+    which2 = mm.mm_lookup(kb2)[1]
+    assert 0 in (which, which2) and -1 in (which, which2)
+    assert k0
+
+
+def test_tuning_disabled_runs_default():
+    mm.check(mm.mm_set_option("tuning", "0"))
+    c = Case(96, 80, 200, dist="int4").device()
+    n0 = mm.mm_candidate_launches(0)
+    mm.check(execute(c))
+    c.check(exact=True)
+    assert mm.mm_candidate_launches(0) == n0 + 1
+    assert mm.mm_cache_size() == 0 and mm.mm_get_stats()["tunes"] == 0
+
+
+@pytest.mark.parametrize("mode", ["error", "nan"])
+def test_fault_injected_candidate_is_excluded(mode):
+    mm.check(mm.mm_set_option("fault", f"gemv_n:{mode}"))
+    c = Case(1, 512, 512, dist="int4").device()
+    mm.check(execute(c))
+    c.check(exact=True)
+    st, kb, _ = mm.mm_tune_key(1, 512, 512, 512, 512, 512, (BF16, BF16, F32), "NN")
+    assert NAMES[mm.mm_lookup(kb)[1]] != "gemv_n"
+
+
+def test_numerical_check_excludes_wrong_candidate():
+    mm.check(mm.mm_set_option("numerical_check", "1e-3_1e-3"))
+    mm.check(mm.mm_set_option("fault", "gemv_n:wrong"))
+    c = Case(1, 512, 512, dist="int4").device()
+    mm.check(execute(c))
+    c.check(exact=True)
+    st, kb, _ = mm.mm_tune_key(1, 512, 512, 512, 512, 512, (BF16, BF16, F32), "NN")
+    assert NAMES[mm.mm_lookup(kb)[1]] != "gemv_n"
+
+
+def test_numerical_check_keeps_correct_candidates():
+    mm.check(mm.mm_set_option("numerical_check", "1e-3_1e-3"))
+    c = Case(1, 512, 512, dist="int4").device()
+    mm.check(execute(c))
+    st, kb, _ = mm.mm_tune_key(1, 512, 512, 512, 512, 512, (BF16, BF16, F32), "NN")
+    assert NAMES[mm.mm_lookup(kb)[1]] == "gemv_n"
+
+
+def test_decision_log(tmp_path):
+    path = str(tmp_path / "decisions.jsonl")
+    mm.check(mm.mm_set_option("decisions", path))
+    c = Case(256, 256, 256, dist="int4").device()
+    mm.check(execute(c))
+    rec = json.loads(open(path).read().splitlines()[-1])
+    assert rec["fastest"] == NAMES[rec["fastest_index"]]
+    assert "m=256 n=256 k=256" in rec["key"]
+    assert rec["limit_ns"] > 0 and rec["bounds"]["compute"]["amount"] == 256 * 256 * 511
+    measured = [x for x in rec["candidates"] if x["state"] == "ok"]
+    assert measured and all(x["n"] >= 1 for x in measured)
+
+
+def test_host_buffers_entry_point():
+    c = Case(37, 45, 130, layout="TN", dt=(BF16, BF16, F32), dist="int4", pad=(3, 0, 5))
+    out = c.C.buf.copy()
+    st = mm.mm_autotune_execute_host(c.A.buf, c.B.buf, out, 37, 45, 130, c.A.ld, c.B.ld, c.C.ld,
+                                     c.dt, "TN")
+    mm.check(st)
+    assert padding_untouched(c.C, out)
+    got = logical_out(c.C, out)
+    want = oracle.round_out(c.c64, F32)
+    assert np.array_equal(got, want)
+
+
+def test_plan_matches_oracle_and_has_naive_last():
+    probs = [(1, 4096, 4096, "NN"), (16, 4096, 4096, "NT"), (256, 256, 256, "NN"),
+             (4097, 4096, 4096, "NN"), (128, 128, 65536, "NN"), (3, 5, 7, "TT")]
+    for M, N, K, lay in probs:
+        at, bt = lay[0] == "T", lay[1] == "T"
+        lda, ldb = (M if at else K), (K if bt else N)
+        items = mm.mm_plan(M, N, K, lda, ldb, N, (BF16, BF16, F32), lay)
+        cands = [dict(index=it["cand"], group=mm.mm_group_name(it["group"]),
+                      group_prio=it["group_prio"], prio=it["prio"],
+                      supported=bool(it["supported"])) for it in items]
+        want = oplan.make_plan(sorted(cands, key=lambda d: d["index"]))
+        got = []
+        for it in items:
+            g = mm.mm_group_name(it["group"])
+            if not got or got[-1][0] != g:
+                got.append((g, []))
+            tiers = got[-1][1]
+            while len(tiers) <= it["tier"]:
+                tiers.append([])
+            tiers[it["tier"]].append(it["cand"])
+        assert got == want, (M, N, K, lay)
+        assert items[-1]["cand"] == 0  # the default closes every plan
+    # lda = 4100 bf16 (stride factor 3): gemv still supported for M <= 16
+    items = mm.mm_plan(16, 4096, 4096, 4100, 4096, 4096, (BF16, BF16, F32), "NN")
+    first = items[0]
+    assert mm.mm_group_name(first["group"]) == "gemv" and first["supported"]
+
+
+def test_concurrent_callers_tune_once():
+    cs = [Case(200, 136, 512, dist="int4", seed=5).device() for _ in range(4)]
+    errs = []
+
+    def work(c):
+        import torch
+        torch.cuda.set_device(0)
+        st = mm.mm_autotune_execute(*c.args())
+        if st != 0:
+            errs.append(mm.mm_last_error())
+
+    ts = [threading.Thread(target=work, args=(c,)) for c in cs]
+    for t in ts:
+        t.start()
+    for t in ts:
+        t.join()
+    assert not errs
+    for c in cs:
+        c.check(exact=True)
+    assert mm.mm_get_stats()["tunes"] == 1
+
+
+def test_large_gemv_workload_selects_gemv():
+    c = Case(1, 4096, 4096, dt=(BF16, BF16, BF16), dist="int4").device()
+    mm.check(execute(c))
+    c.check(exact=True)
+    st, kb, _ = mm.mm_tune_key(1, 4096, 4096, 4096, 4096, 4096, (BF16, BF16, BF16), "NN")
+    assert NAMES[mm.mm_lookup(kb)[1]] == "gemv_n"
+
+
+def test_misaligned_lda_workload_key_sharing():
+    """lda = 4100 (stride factor 3); M = 4097 and 8192 share one key, so the
+    second call is a hit."""
+    c1 = Case(4097, 4096, 4096, dt=(BF16, BF16, F32), dist="int4", pad=(4, 0, 0))
+    c2 = Case(8192, 4096, 4096, dt=(BF16, BF16, F32), dist="int4", pad=(4, 0, 0))
+    st, k1, _ = mm.mm_tune_key(4097, 4096, 4096, 4100, 4096, 4096, (BF16, BF16, F32), "NN")
+    st, k2, _ = mm.mm_tune_key(8192, 4096, 4096, 4100, 4096, 4096, (BF16, BF16, F32), "NN")
+    assert k1 == k2
+    mm.check(mm.mm_set_option("max_tuning_iterations", "3"))
+    c1.device()
+    mm.check(execute(c1))
+    del c1
+    c2.device()
+    before = mm.mm_get_stats()["hits"]
+    mm.check(execute(c2))
+    assert mm.mm_get_stats()["hits"] == before + 1
+    # sampled outputs against the oracle (full oracle would take minutes)
+    import torch
+    torch.cuda.synchronize()
+    flat = c2.result()
+    rng = np.random.default_rng(0)
+    pts = np.stack([np.zeros(400, dtype=np.int64), rng.integers(0, 8192, 400),
+                    rng.integers(0, 4096, 400)], axis=1)
+    want = oracle.round_out(oracle.gemm_points(c2.A, c2.B, 4096, pts), F32)
+    got = flat[pts[:, 1] * c2.C.ld + pts[:, 2]]
+    assert np.array_equal(got, want)
+
+
+def test_graph_capture_miss_uses_default():
+    import torch
+    c = Case(48, 40, 72, dist="int4").device()
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    n0 = mm.mm_candidate_launches(0)
+    with torch.cuda.graph(g, stream=s):
+        st = mm.mm_autotune_execute(*c.args(), stream=s)
+    assert st == 0, mm.mm_last_error()
+    g.replay()
+    torch.cuda.synchronize()
+    c.check(exact=True)
+    assert mm.mm_get_stats()["tunes"] == 0
+    assert mm.mm_candidate_launches(0) == n0 + 1
