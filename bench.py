@@ -221,16 +221,31 @@ def ensure_built():
     mod.build()
 
 
+def kernel_source(kernel_name):
+    """The source file that holds a candidate's kernel."""
+    kdir = os.path.join(ROOT, "matmul_selection_gb300", "csrc", "kernels")
+    if kernel_name.startswith("tc_"):
+        return os.path.join(kdir, "tc_gemm.cu")
+    if kernel_name.startswith("gemv"):
+        return os.path.join(kdir, "gemv.cu")
+    return os.path.join(kdir, "naive.cu")
+
+
 def traffic_for(kernel_name, workload):
-    """DRAM bytes per launch from a committed ncu summary of the same build."""
+    """DRAM bytes per launch from a committed ncu summary, or None when the
+    kernel's source changed since the counters were taken."""
+    import hashlib
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
-    import matmul_selection_gb300 as mm
     with open(path) as f:
         d = json.load(f)
     e = d.get(f"{kernel_name}@{workload}")
-    if not e or e.get("build") != mm.mm_version():
+    if not e:
+        return None
+    with open(kernel_source(kernel_name), "rb") as f:
+        sha = hashlib.sha1(f.read()).hexdigest()[:12]
+    if e.get("source_sha1") != sha:
         return None
     return e.get("dram_bytes_per_launch")
 
