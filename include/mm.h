@@ -238,6 +238,30 @@ const char *mm_last_error(void);
 /* Library version string ("<semver>+<build fingerprint>"). */
 const char *mm_version(void);
 
+/*
+ * mm_splitk_gemm_noalloc -- C = A.B (batch 1) with the split-K tensor-core
+ * kernel, allocating nothing.  No counterpart in the pages this library
+ * follows: it serves callers that may not call cudaMalloc/cudaFree -- a
+ * server that reserves all device memory for its own pool at start-up, a
+ * plugin inside a framework that owns the allocator, a latency-bound loop
+ * that cannot take the implicit device synchronisation of an allocation.
+ * Arguments are those of mm_autotune_execute without the batch; lhs, rhs and
+ * out are device pointers the caller owns; the call is asynchronous on
+ * `stream`.  The K-slice partial sums go to a fixed 16 MiB workspace that is
+ * part of the library's device image (held on every GPU that loads the
+ * library until exit): M*N must be at most 2,097,120 (two fp32 slices), else
+ * MM_ERR_INVALID_ARG with the limit in the message.  The first call on a
+ * device resolves the workspace's device address (cudaGetSymbolAddress) with
+ * that device current; make it before any stream capture.  All calls share
+ * the workspace, so calls whose GPU execution overlaps (two streams, two
+ * threads) race and must be ordered by the caller.  Alignment and type rules
+ * are those of the tensor-core candidates (16-byte aligned A, B and leading
+ * dimensions; f32 only as NT), else MM_ERR_UNSUPPORTED.
+ */
+mm_status mm_splitk_gemm_noalloc(const void *lhs, const void *rhs, void *out, int64_t M,
+                                 int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
+                                 mm_dtypes dt, mm_layout layout, void *stream);
+
 /* Free every library-owned device buffer and the tables; saves the table of
  * each device to MM_CACHE_FILE first when that option is set and tuning
  * produced new entries.  The library may be used again afterwards. */

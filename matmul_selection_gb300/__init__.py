@@ -95,6 +95,8 @@ _sig = {
     "mm_last_error": (_cp, []),
     "mm_version": (_cp, []),
     "mm_shutdown": (None, []),
+    "mm_splitk_gemm_noalloc": (_i32, [_vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64, _i64,
+                                      mm_dtypes, ctypes.c_int, _vp]),
 }
 for _name, (_res, _args) in _sig.items():
     _f = getattr(_lib, _name)
@@ -271,6 +273,12 @@ def mm_reset_stats():
 
 def mm_shutdown():
     _lib.mm_shutdown()
+
+
+def mm_splitk_gemm_noalloc(lhs, rhs, out, M, N, K, lda, ldb, ldc, dtypes, layout, stream=None):
+    """Split-K GEMM into the library's fixed workspace: no device allocation."""
+    return _lib.mm_splitk_gemm_noalloc(_ptr(lhs), _ptr(rhs), _ptr(out), M, N, K, lda, ldb, ldc,
+                                       _dt(dtypes), _layout(layout), _stream(stream))
 
 
 def library_handle():

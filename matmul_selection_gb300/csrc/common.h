@@ -246,6 +246,9 @@ mm_status launch_tc(const Problem &p, LaunchCtx &ctx, int cfg);
 int tc_config_count();
 const char *tc_config_name(int cfg);
 bool tc_config_is_splitk(int cfg);
+int tc_config_index(const char *name);
+mm_status launch_tc_splitk_into(const Problem &p, const DeviceInfo &di, int cfg, float *ws,
+                                size_t ws_bytes, int *err, cudaStream_t s);
 
 // ---------------------------------------------------------------- tuner
 struct ExecResult {

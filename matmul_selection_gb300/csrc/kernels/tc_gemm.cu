@@ -611,6 +611,100 @@ void choose_splits(int64_t tiles, int64_t num_kb, int sms, int *splits, int *kb_
 
 }  // namespace
 
+// Split-K launch into a workspace the caller provides (no allocation here).
+// Picks the largest split count <= the usual choice whose fp32 partials fit
+// in ws_bytes; needs at least two K slices.
+mm_status launch_tc_splitk_into(const Problem &p, const DeviceInfo &di, int cfg, float *ws,
+                                size_t ws_bytes, int *err, cudaStream_t s) {
+  std::string why;
+  if (!kCfgs[cfg].splitk) return set_error(MM_ERR_INVALID_ARG, "not a split-K configuration");
+  if (!tc_supports(p, di, cfg, &why))
+    return set_error(MM_ERR_UNSUPPORTED, "%s: %s", kCfgs[cfg].name, why.c_str());
+  const TcCfg &c = kCfgs[cfg];
+  const int es = dtype_bytes(p.ta);
+  const int bk = 128 / es, atom = 128 / es, umma_k = 32 / es;
+  const int bn = c.bn;
+  TcParams tp;
+  std::memset(&tp, 0, sizeof tp);
+  tp.M = (int)p.M;
+  tp.N = (int)p.N;
+  tp.K = (int)p.K;
+  tp.batch = (int)p.batch;
+  tp.tiles_m = (int)ceil_div(p.M, BM);
+  tp.tiles_n = (int)ceil_div(p.N, bn);
+  tp.num_kb = (int)ceil_div(p.K, bk);
+  const int64_t tiles = (int64_t)tp.tiles_m * tp.tiles_n * tp.batch;
+  choose_splits(tiles, tp.num_kb, di.sms, &tp.splits, &tp.kb_per_split);
+  const size_t slice_bytes = (size_t)tp.batch * (size_t)p.M * (size_t)p.N * sizeof(float);
+  const int64_t fit = slice_bytes ? (int64_t)(ws_bytes / slice_bytes) : 0;
+  if (fit < 2)
+    return set_error(MM_ERR_INVALID_ARG,
+                     "problem too large for the fixed workspace: two K slices need %zu bytes, "
+                     "the workspace holds %zu",
+                     2 * slice_bytes, ws_bytes);
+  if (tp.splits > fit) {
+    int64_t per = ceil_div(tp.num_kb, fit);
+    tp.kb_per_split = (int)per;
+    tp.splits = (int)ceil_div(tp.num_kb, per);
+  }
+  if (tp.splits < 2) return set_error(MM_ERR_INVALID_ARG, "split-K needs at least two K slices");
+  const int64_t units = tiles * tp.splits;
+  if (units >= (1LL << 31)) return set_error(MM_ERR_UNSUPPORTED, "too many work units");
+  tp.total_units = (int)units;
+  CUtensorMap ma, mb;
+  mm_status st;
+  if (!p.at)
+    st = encode_map(&ma, p.ta, p.A, p.K, p.M, p.batch, p.lda * es, p.sA * es, bk, BM);
+  else
+    st = encode_map(&ma, p.ta, p.A, p.M, p.K, p.batch, p.lda * es, p.sA * es, atom, bk);
+  if (st != MM_OK) return st;
+  if (p.bt)
+    st = encode_map(&mb, p.tb, p.B, p.K, p.N, p.batch, p.ldb * es, p.sB * es, bk, bn);
+  else
+    st = encode_map(&mb, p.tb, p.B, p.N, p.K, p.batch, p.ldb * es, p.sB * es, atom, bk);
+  if (st != MM_OK) return st;
+  tp.C = p.C;
+  tp.ldc = p.ldc;
+  tp.sC = p.sC;
+  tp.tc = p.tc;
+  const int ec = dtype_bytes(p.tc);
+  tp.c_vec_ok = ((uintptr_t)p.C % 16 == 0) && ((p.ldc * ec) % 16 == 0) &&
+                (p.batch <= 1 || (p.sC * ec) % 16 == 0);
+  tp.err = err;
+  tp.timeout_ns = kWaitTimeoutNs;
+  tp.a_mn = p.at ? 1 : 0;
+  tp.b_mn = p.bt ? 0 : 1;
+  const uint32_t fmt = p.ta == MM_F16 ? 0u : p.ta == MM_BF16 ? 1u : 2u;
+  tp.idesc = (1u << 4) | (fmt << 7) | (fmt << 10) | ((uint32_t)tp.a_mn << 15) |
+             ((uint32_t)tp.b_mn << 16) | ((uint32_t)(bn >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+  const uint32_t mn_atom_bytes = (uint32_t)bk * 128u;
+  tp.a_desc = tp.a_mn ? smem_desc_bits(mn_atom_bytes, 1024) : smem_desc_bits(16, 1024);
+  tp.b_desc = tp.b_mn ? smem_desc_bits(mn_atom_bytes, 1024) : smem_desc_bits(16, 1024);
+  tp.a_kstep = tp.a_mn ? (uint32_t)(umma_k * 128) >> 4 : 32u >> 4;
+  tp.b_kstep = tp.b_mn ? (uint32_t)(umma_k * 128) >> 4 : 32u >> 4;
+  tp.a_boxes = tp.a_mn ? BM / atom : 1;
+  tp.b_boxes = tp.b_mn ? bn / atom : 1;
+  tp.a_box_stride = mn_atom_bytes;
+  tp.b_box_stride = mn_atom_bytes;
+  tp.ws = ws;
+  const int grid = (int)std::min<int64_t>(units, di.sms);
+  st = es == 2 ? dispatch<2>(cfg, ma, mb, tp, grid, s) : dispatch<4>(cfg, ma, mb, tp, grid, s);
+  if (st != MM_OK) return st;
+  const int64_t total = (int64_t)tp.batch * p.M * p.N;
+  int blocks = (int)std::min<int64_t>(ceil_div(total, 256), (int64_t)di.sms * 8);
+  splitk_reduce_kernel<<<blocks, 256, 0, s>>>(tp.ws, tp.splits, tp.batch, tp.M, tp.N, p.C, p.tc,
+                                               p.ldc, p.sC);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_error(e, "splitk_reduce_kernel launch");
+  return MM_OK;
+}
+
+int tc_config_index(const char *name) {
+  for (int i = 0; i < tc_config_count(); ++i)
+    if (std::strcmp(kCfgs[i].name, name) == 0) return i;
+  return -1;
+}
+
 int tc_config_count() { return (int)(sizeof kCfgs / sizeof kCfgs[0]); }
 const char *tc_config_name(int cfg) { return kCfgs[cfg].name; }
 bool tc_config_is_splitk(int cfg) { return kCfgs[cfg].splitk; }
