@@ -162,7 +162,7 @@ mm_status cache_load(DeviceState &ds, const std::string &path) {
     }
     if (std::find(e.ranking.begin(), e.ranking.end(), 0) == e.ranking.end()) e.ranking.push_back(0);
     e.from_file = true;
-    ds.table[k] = e;
+    ds.table[k] = std::make_shared<const TableEntry>(e);
   }
   return MM_OK;
 }
@@ -172,7 +172,7 @@ mm_status cache_save(DeviceState &ds, const std::string &path) {
   {
     std::shared_lock<std::shared_mutex> lk(ds.table_mu);
     for (const auto &kv : ds.table) {
-      const TableEntry &e = kv.second;
+      const TableEntry &e = *kv.second;
       char ms[64];
       snprintf(ms, sizeof ms, "%.6g", e.median_ms);
       lines.push_back("MatmulKey," + csv_field(key_text(kv.first)) + "," +

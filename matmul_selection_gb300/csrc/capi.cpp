@@ -184,7 +184,7 @@ mm_status mm_lookup(const mm_key *key, int32_t *index) {
   std::shared_lock<std::shared_mutex> lk(ds->table_mu);
   auto it = ds->table.find(k);
   if (it == ds->table.end()) return set_error(MM_ERR_NOT_FOUND, "key not in the table");
-  *index = it->second.winner;
+  *index = it->second->winner;
   return MM_OK;
 }
 

@@ -119,7 +119,7 @@ struct Options {
   std::string fault;
 };
 // Snapshot of the current options (env values take precedence over the API).
-Options get_options();
+const Options &get_options();
 mm_status set_option(const std::string &name, const std::string &value);
 mm_status get_option(const std::string &name, std::string *value);
 
@@ -170,7 +170,7 @@ struct DeviceState {
   std::mutex stage_mu;
   // tuning table
   std::shared_mutex table_mu;
-  std::unordered_map<KeyPod, TableEntry, KeyHash, KeyEq> table;
+  std::unordered_map<KeyPod, std::shared_ptr<const TableEntry>, KeyHash, KeyEq> table;
   std::mutex pending_mu;
   std::condition_variable pending_cv;
   std::unordered_set<KeyPod, KeyHash, KeyEq> pending;

@@ -481,6 +481,293 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (warp == 1) tmem_dealloc(tmem_base, TMEM_COLS);
 }
 
+// ---------------------------------------------------------------- 2-SM kernel
+// The same pipeline on a CTA pair (cluster of 2) with tcgen05.mma.cta_group::2:
+// one MMA instruction computes a 256 x BN tile; each CTA holds 128 rows of A
+// and half of the B tile (BN/2 columns) in its own shared memory and receives
+// its 128 rows of the accumulator (all BN columns) in its own TMEM.  Only the
+// pair's even CTA (the leader) issues MMAs.  Both CTAs' TMA loads complete on
+// the leader's "full" barrier (tx = both halves); the leader's commits are
+// multicast to the "empty" and "tmem full" barriers of both CTAs; both CTAs'
+// epilogue warps arrive on the leader's "tmem empty" barrier.  Each SM thus
+// loads half as many B bytes per k-block as the single-SM form.
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_id_x() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t nclusters_x() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+  return r;
+}
+// Shared::cluster address of the same shared-memory offset in CTA `rank`.
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+               : "memory");
+}
+__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap *map,
+                                                 uint32_t leader_bar, int c0, int c1, int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.cta_group::2"
+      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(leader_bar), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish_pair() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+template <int ES>
+__device__ __forceinline__ void umma_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                          uint32_t idesc, uint32_t accumulate) {
+  if constexpr (ES == 2) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+  } else {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+  }
+}
+// Arrive on the barrier at this offset in both CTAs of the pair once every
+// tcgen05 op issued so far by this thread has completed.
+__device__ __forceinline__ void umma_commit_pair_both(uint32_t bar) {
+  const uint16_t mask = 0x3;
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(bar),
+      "h"(mask)
+      : "memory");
+}
+__device__ __forceinline__ void umma_commit_pair_local(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   bar)
+               : "memory");
+}
+
+constexpr uint32_t kPairSlack = 16384;  // shared memory after the ring (over-read guard)
+
+template <int BN, int STAGES, int ES>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    tc2_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
+                    const __grid_constant__ CUtensorMap tmB, const TcParams p) {
+  constexpr int BNH = BN / 2;                 // B columns held by each CTA
+  constexpr uint32_t A_BYTES = BM * 128;
+  constexpr uint32_t B_BYTES = BNH * 128;
+  constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+  constexpr uint32_t PAIR_TX = 2 * STAGE_BYTES;
+  constexpr int BK = 128 / ES;
+  constexpr int UMMA_K = 32 / ES;
+  constexpr int KSTEPS = BK / UMMA_K;
+  constexpr uint32_t TMEM_COLS = 2 * BN;
+  constexpr int ATOM = 128 / ES;
+  constexpr int PAIR_M = 2 * BM;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                              ~static_cast<uintptr_t>(1023));
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + STAGES * STAGE_BYTES + kPairSlack);
+  const uint32_t full0 = smem_u32(bars);
+  const uint32_t empty0 = full0 + 8 * STAGES;
+  const uint32_t tfull0 = empty0 + 8 * STAGES;
+  const uint32_t tempty0 = tfull0 + 16;
+  const uint32_t drain = tempty0 + 16;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * STAGES + 5);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+  const int cid = (int)cluster_id_x(), ncl = (int)nclusters_x();
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(tfull0 + 8 * a, 1);
+      mbar_init(tempty0 + 8 * a, 8);  // 4 epilogue warps in each CTA of the pair
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(smem_u32(tmem_slot), TMEM_COLS);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  cluster_sync_all();  // barriers of both CTAs initialised before any remote use
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const uint32_t leader_full0 = map_to_rank(full0, 0);
+  const uint32_t leader_tempty0 = map_to_rank(tempty0, 0);
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer (both CTAs)
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int u = cid; u < p.total_units && ok; u += ncl) {
+        int tm, tn, b, sp;
+        decode_unit(p, u, tm, tn, b, sp);
+        const int m0 = tm * PAIR_M + (int)rank * BM;
+        const int n0 = tn * BN + (int)rank * BNH;
+        for (int kb = 0; kb < p.num_kb; ++kb) {
+          if (!wait_bounded(empty0 + 8 * stage, phase ^ 1, abort_flag, p.err, kErrProducer,
+                            p.timeout_ns)) {
+            ok = false;
+            break;
+          }
+          const uint32_t lfb = leader_full0 + 8 * stage;
+          const uint32_t sa = smem_u32(smem + stage * STAGE_BYTES);
+          const uint32_t sb = sa + A_BYTES;
+          if (leader) mbar_expect_tx(full0 + 8 * stage, PAIR_TX);
+          if (!p.a_mn) {
+            tma_load_3d_pair(sa, &tmA, lfb, kb * BK, m0, b);
+          } else {
+            for (int j = 0; j < p.a_boxes; ++j)
+              tma_load_3d_pair(sa + j * p.a_box_stride, &tmA, lfb, m0 + j * ATOM, kb * BK, b);
+          }
+          if (!p.b_mn) {
+            tma_load_3d_pair(sb, &tmB, lfb, kb * BK, n0, b);
+          } else {
+            for (int j = 0; j < p.b_boxes; ++j)
+              tma_load_3d_pair(sb + j * p.b_box_stride, &tmB, lfb, n0 + j * ATOM, kb * BK, b);
+          }
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      // the leader's full barriers see both CTAs' copies land
+      if (leader)
+        for (int s = 0; s < STAGES; ++s) {
+          int st = (stage + s) % STAGES;
+          uint32_t par = (st < stage) ? phase : phase ^ 1;
+          wait_drain(full0 + 8 * st, par, p.err, kErrProducer, p.timeout_ns);
+        }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer (leader)
+    if (lane == 0 && leader) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int u = cid; u < p.total_units && ok; u += ncl) {
+        if (!wait_bounded(tempty0 + 8 * acc, acc_phase ^ 1, abort_flag, p.err, kErrMma,
+                          p.timeout_ns))
+          break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+        for (int kb = 0; kb < p.num_kb; ++kb) {
+          if (!wait_bounded(full0 + 8 * stage, phase, abort_flag, p.err, kErrMma, p.timeout_ns)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(smem + stage * STAGE_BYTES);
+          const uint32_t sb = sa + A_BYTES;
+          const uint64_t adesc = p.a_desc | (uint64_t)((sa >> 4) & 0x3FFFu);
+          const uint64_t bdesc = p.b_desc | (uint64_t)((sb >> 4) & 0x3FFFu);
+#pragma unroll
+          for (int kk = 0; kk < KSTEPS; ++kk)
+            umma_pair<ES>(d_tmem, adesc + (uint64_t)(kk * p.a_kstep),
+                          bdesc + (uint64_t)(kk * p.b_kstep), p.idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+          umma_commit_pair_both(empty0 + 8 * stage);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (!ok) break;
+        umma_commit_pair_both(tfull0 + 8 * acc);
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1;
+        }
+      }
+      umma_commit_pair_local(drain);
+      wait_drain(drain, 0, p.err, kErrDrain, p.timeout_ns);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue (both CTAs)
+    const int q = warp & 3;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int u = cid; u < p.total_units; u += ncl) {
+      int tm, tn, b, sp;
+      decode_unit(p, u, tm, tn, b, sp);
+      int ok = 1;
+      if (lane == 0)
+        ok = wait_bounded(tfull0 + 8 * acc, acc_phase, abort_flag, p.err, kErrEpilogue,
+                          p.timeout_ns);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      tc_fence_after();
+      const int row = tm * PAIR_M + (int)rank * BM + q * 32 + lane;
+      const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld_32cols(tbase + (uint32_t)(c * 32), r);
+        tmem_ld_wait();
+        store_chunk(p, b, 0, row, tn * BN + c * 32, r);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(leader_tempty0 + 8 * acc);
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1;
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();  // the leader's MMAs (reading both CTAs' smem, writing both TMEMs) are done
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc_pair(tmem_base, TMEM_COLS);
+}
+
 // Sum the split-K partials in increasing slice order and convert.
 __global__ void splitk_reduce_kernel(const float *__restrict__ ws, int S, int batch, int M, int N,
                                      void *C, int tc, int64_t ldc, int64_t sC) {
@@ -505,21 +792,29 @@ __global__ void splitk_reduce_kernel(const float *__restrict__ ws, int S, int ba
 // ---------------------------------------------------------------- host side
 struct TcCfg {
   const char *name;
-  int bn;
+  int bn;       // tile N (for a pair: the pair's tile N, each CTA loads half of B)
   int stages;
   bool splitk;
+  bool pair;    // 2-SM (cta_group::2) kernel, tile M = 256
 };
 
 const TcCfg kCfgs[] = {
-    {"tc_128x256_s4", 256, 4, false},
-    {"tc_128x128_s6", 128, 6, false},
-    {"tc_128x64_s8", 64, 8, false},
-    {"tc_splitk_128x128_s6", 128, 6, true},
-    {"tc_splitk_128x64_s8", 64, 8, true},
+    {"tc_128x256_s4", 256, 4, false, false},
+    {"tc_128x128_s6", 128, 6, false, false},
+    {"tc_128x64_s8", 64, 8, false, false},
+    {"tc_splitk_128x128_s6", 128, 6, true, false},
+    {"tc_splitk_128x64_s8", 64, 8, true, false},
+    {"tc2_256x256_s6", 256, 6, false, true},
+    {"tc2_256x128_s8", 128, 8, false, true},
 };
 
 size_t smem_bytes(int bn, int stages) {
   return (size_t)stages * (BM * 128 + bn * 128) + 1024 + 256;
+}
+
+size_t smem_bytes_cfg(const TcCfg &c) {
+  if (!c.pair) return smem_bytes(c.bn, c.stages);
+  return (size_t)c.stages * (BM * 128 + (c.bn / 2) * 128) + kPairSlack + 1024 + 256;
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -585,6 +880,50 @@ mm_status launch_kernel(const CUtensorMap &ma, const CUtensorMap &mb, const TcPa
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_error(e, "tc_gemm_kernel launch");
   return MM_OK;
+}
+
+template <int BN, int STAGES, int ES>
+mm_status launch_pair_kernel(const CUtensorMap &ma, const CUtensorMap &mb, const TcParams &tp,
+                             int64_t units, cudaStream_t s) {
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  static int max_clusters = 0;
+  const TcCfg cfg_shape{"", BN, STAGES, false, true};
+  const size_t smem = smem_bytes_cfg(cfg_shape);
+  auto kern = tc2_gemm_kernel<BN, STAGES, ES>;
+  cudaLaunchConfig_t lc = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  lc.blockDim = dim3(kTcThreads);
+  lc.dynamicSmemBytes = smem;
+  lc.stream = s;
+  lc.attrs = attr;
+  lc.numAttrs = 1;
+  std::call_once(once, [&] {
+    attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (attr_err == cudaSuccess) {
+      cudaLaunchConfig_t q = lc;
+      q.gridDim = dim3(2);
+      attr_err = cudaOccupancyMaxActiveClusters(&max_clusters, kern, &q);
+    }
+  });
+  if (attr_err != cudaSuccess) return cuda_error(attr_err, "tc2 kernel set-up");
+  if (max_clusters < 1) return set_error(MM_ERR_UNSUPPORTED, "no CTA pair fits on this device");
+  const int64_t clusters = std::min<int64_t>(units, max_clusters);
+  lc.gridDim = dim3((unsigned)(2 * clusters));
+  cudaError_t e = cudaLaunchKernelEx(&lc, kern, ma, mb, tp);
+  if (e != cudaSuccess) return cuda_error(e, "tc2_gemm_kernel launch");
+  return MM_OK;
+}
+
+template <int ES>
+mm_status dispatch_pair(int cfg, const CUtensorMap &ma, const CUtensorMap &mb,
+                        const TcParams &tp, int64_t units, cudaStream_t s) {
+  if (kCfgs[cfg].bn == 256) return launch_pair_kernel<256, 6, ES>(ma, mb, tp, units, s);
+  return launch_pair_kernel<128, 8, ES>(ma, mb, tp, units, s);
 }
 
 template <int ES>
@@ -732,7 +1071,7 @@ bool tc_supports(const Problem &p, const DeviceInfo &d, int cfg, std::string *wh
   if (p.lda * es >= (1LL << 40) || p.ldb * es >= (1LL << 40) || p.sA * es >= (1LL << 40) ||
       p.sB * es >= (1LL << 40))
     return no("stride too large for TMA");
-  if ((int64_t)smem_bytes(c.bn, c.stages) > d.smem_optin) return no("not enough shared memory");
+  if ((int64_t)smem_bytes_cfg(c) > d.smem_optin) return no("not enough shared memory");
   if (c.splitk) {
     const int64_t num_kb = ceil_div(p.K, 128 / es);
     if (num_kb < 2) return no("split-K needs at least two K blocks");
@@ -748,6 +1087,8 @@ mm_status launch_tc(const Problem &p, LaunchCtx &ctx, int cfg) {
   const int es = dtype_bytes(p.ta);
   const int bk = 128 / es, atom = 128 / es, umma_k = 32 / es;
   const int bn = c.bn;
+  const int bn_cta = c.pair ? bn / 2 : bn;  // B columns one CTA loads
+  const int tile_m = c.pair ? 2 * BM : BM;
   CUtensorMap ma, mb;
   mm_status st;
   // A: logical M x K.  K-major when stored row-major (N), MN-major when T.
@@ -758,7 +1099,7 @@ mm_status launch_tc(const Problem &p, LaunchCtx &ctx, int cfg) {
   if (st != MM_OK) return st;
   // B: logical K x N.  K-major when stored transposed (T), MN-major when N.
   if (p.bt)
-    st = encode_map(&mb, p.tb, p.B, p.K, p.N, p.batch, p.ldb * es, p.sB * es, bk, bn);
+    st = encode_map(&mb, p.tb, p.B, p.K, p.N, p.batch, p.ldb * es, p.sB * es, bk, bn_cta);
   else
     st = encode_map(&mb, p.tb, p.B, p.N, p.K, p.batch, p.ldb * es, p.sB * es, atom, bk);
   if (st != MM_OK) return st;
@@ -769,7 +1110,7 @@ mm_status launch_tc(const Problem &p, LaunchCtx &ctx, int cfg) {
   tp.N = (int)p.N;
   tp.K = (int)p.K;
   tp.batch = (int)p.batch;
-  tp.tiles_m = (int)ceil_div(p.M, BM);
+  tp.tiles_m = (int)ceil_div(p.M, tile_m);
   tp.tiles_n = (int)ceil_div(p.N, bn);
   tp.num_kb = (int)ceil_div(p.K, bk);
   const int64_t tiles = (int64_t)tp.tiles_m * tp.tiles_n * tp.batch;
@@ -799,7 +1140,7 @@ mm_status launch_tc(const Problem &p, LaunchCtx &ctx, int cfg) {
              | ((uint32_t)tp.a_mn << 15)      // A major (1 = MN)
              | ((uint32_t)tp.b_mn << 16)      // B major (1 = MN)
              | ((uint32_t)(bn >> 3) << 17)    // N / 8
-             | ((uint32_t)(BM >> 4) << 24);   // M / 16
+             | ((uint32_t)(tile_m >> 4) << 24);  // M / 16 (256 for a CTA pair)
   // K-major: 8-row groups 1024 B apart, K advances 32 B inside the swizzle row.
   // MN-major: boxes of 128 bytes x bk rows; atoms along MN are bk*128 B apart,
   // 8-row K groups 1024 B apart, K advances umma_k rows (umma_k * 128 B).
@@ -809,9 +1150,12 @@ mm_status launch_tc(const Problem &p, LaunchCtx &ctx, int cfg) {
   tp.a_kstep = tp.a_mn ? (uint32_t)(umma_k * 128) >> 4 : 32u >> 4;
   tp.b_kstep = tp.b_mn ? (uint32_t)(umma_k * 128) >> 4 : 32u >> 4;
   tp.a_boxes = tp.a_mn ? BM / atom : 1;
-  tp.b_boxes = tp.b_mn ? bn / atom : 1;
+  tp.b_boxes = tp.b_mn ? bn_cta / atom : 1;
   tp.a_box_stride = mn_atom_bytes;
   tp.b_box_stride = mn_atom_bytes;
+  if (c.pair)
+    return es == 2 ? dispatch_pair<2>(cfg, ma, mb, tp, units, ctx.stream)
+                   : dispatch_pair<4>(cfg, ma, mb, tp, units, ctx.stream);
   if (tp.splits > 1) {
     void *w = nullptr;
     size_t ws_bytes = (size_t)tp.splits * tp.batch * (size_t)p.M * p.N * sizeof(float);

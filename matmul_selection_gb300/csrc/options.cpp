@@ -121,12 +121,27 @@ std::string show(const Options &o, const std::string &n) {
 
 }  // namespace
 
-Options get_options() {
+std::atomic<uint64_t> g_version{1};
+
+Options snapshot() {
   std::call_once(g_env_once, read_env);
   std::lock_guard<std::mutex> lk(g_mu);
   Options o = g_api;
   for (const auto &kv : g_env) apply(o, kv.first, kv.second);  // env wins
   return o;
+}
+
+// Each thread keeps a copy that is refreshed when an option changes, so the
+// warm path reads options without a lock or a string copy.
+const Options &get_options() {
+  thread_local uint64_t seen = 0;
+  thread_local Options cached;
+  uint64_t v = g_version.load(std::memory_order_acquire);
+  if (v != seen) {
+    cached = snapshot();
+    seen = v;
+  }
+  return cached;
 }
 
 mm_status set_option(const std::string &name, const std::string &value) {
@@ -138,6 +153,7 @@ mm_status set_option(const std::string &name, const std::string &value) {
     return set_error(MM_ERR_INVALID_ARG, "bad value '%s' for option '%s'", value.c_str(),
                      name.c_str());
   g_api = o;
+  g_version.fetch_add(1, std::memory_order_release);
   return MM_OK;
 }
 

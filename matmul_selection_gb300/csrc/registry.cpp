@@ -168,8 +168,8 @@ mm_status launch_candidate(int index, const Problem &p, LaunchCtx &ctx) {
   std::string why;
   if (!c.supports(p, ctx.dev->info, c.cfg, &why))
     return set_error(MM_ERR_UNSUPPORTED, "%s: %s", c.name.c_str(), why.c_str());
-  Options o = get_options();
-  if (fault_error(o.fault, c.name))
+  const Options &o = get_options();
+  if (!o.fault.empty() && fault_error(o.fault, c.name))
     return set_error(MM_ERR_CUDA, "%s: injected launch error", c.name.c_str());
   mm_status st = c.launch(p, ctx, c.cfg);
   if (st == MM_OK) count_launch(index, ctx.tuning);

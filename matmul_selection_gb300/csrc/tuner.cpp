@@ -522,17 +522,17 @@ mm_status autotune_execute(const Problem &p, cudaStream_t s, ExecResult *res) {
     if (res) res->candidate = 0;
     return launch_candidate(0, p, ctx);
   }
-  Options o = get_options();
+  const Options &o = get_options();
   KeyPod key = make_key(p, o.level);
   {
     std::shared_lock<std::shared_mutex> lk(ds.table_mu);
     auto it = ds.table.find(key);
     if (it != ds.table.end()) {
-      TableEntry e = it->second;
+      std::shared_ptr<const TableEntry> e = it->second;
       lk.unlock();
       stats().hits.fetch_add(1, std::memory_order_relaxed);
       if (res) res->hit = true;
-      return run_entry(ds, e, p, s, res);
+      return run_entry(ds, *e, p, s, res);
     }
   }
   stats().misses.fetch_add(1, std::memory_order_relaxed);
@@ -554,10 +554,10 @@ mm_status autotune_execute(const Problem &p, cudaStream_t s, ExecResult *res) {
     std::shared_lock<std::shared_mutex> lk(ds.table_mu);
     auto it = ds.table.find(key);
     if (it != ds.table.end()) {
-      TableEntry e = it->second;
+      std::shared_ptr<const TableEntry> e = it->second;
       lk.unlock();
       if (res) res->hit = true;
-      return run_entry(ds, e, p, s, res);
+      return run_entry(ds, *e, p, s, res);
     }
   }
   // pending protocol: one tuner per key; others wait (bounded)
@@ -569,9 +569,9 @@ mm_status autotune_execute(const Problem &p, cudaStream_t s, ExecResult *res) {
       std::shared_lock<std::shared_mutex> lk(ds.table_mu);
       auto it = ds.table.find(key);
       if (it != ds.table.end()) {
-        TableEntry e = it->second;
+        std::shared_ptr<const TableEntry> e = it->second;
         lk.unlock();
-        return run_entry(ds, e, p, s, res);
+        return run_entry(ds, *e, p, s, res);
       }
       if (res) res->candidate = 0;
       return launch_candidate(0, p, ctx);
@@ -590,7 +590,7 @@ mm_status autotune_execute(const Problem &p, cudaStream_t s, ExecResult *res) {
     std::lock_guard<std::mutex> pl(ds.pending_mu);
     if (st == MM_OK) {
       std::unique_lock<std::shared_mutex> lk(ds.table_mu);
-      ds.table[key] = entry;
+      ds.table[key] = std::make_shared<const TableEntry>(entry);
       ds.dirty = true;
     }
     ds.pending.erase(key);
