@@ -18,6 +18,7 @@ workload, each step a bounded sample of output elements.
 from __future__ import annotations
 
 import argparse
+import ctypes
 import csv
 import io
 import json
@@ -282,13 +283,19 @@ def run_ours(args, w, name, rank, world, peaks, quiet=False):
     if forced:
         idx = mm.candidate_names().index(forced)
 
+    # arguments converted to C types once, so a step costs one foreign call
+    lib = mm.library_handle()
+    cdt = mm.mm_dtypes(*dt)
+    clay = mm.LAYOUTS[w["layout"]]
+    cb = None if b is None else ctypes.byref(mm.mm_batch(*b))
+    ptrs = [(s_[0].data_ptr(), s_[1].data_ptr(), s_[2].data_ptr()) for s_ in sets]
+
     def call(s):
-        dA, dB, dC = sets[s % R]
+        pa, pb, pc = ptrs[s % R]
         if forced:
-            return mm.mm_execute_candidate(idx, dA, dB, dC, M, N, K, A.ld, B.ld, C.ld, dt,
-                                           w["layout"], b, sh)
-        return mm.mm_autotune_execute(dA, dB, dC, M, N, K, A.ld, B.ld, C.ld, dt, w["layout"], b,
-                                      sh)
+            return lib.mm_execute_candidate(idx, pa, pb, pc, M, N, K, A.ld, B.ld, C.ld, cdt, clay,
+                                            cb, sh)
+        return lib.mm_autotune_execute(pa, pb, pc, M, N, K, A.ld, B.ld, C.ld, cdt, clay, cb, sh)
 
     torch.cuda.synchronize()
     mm.mm_cache_clear()
@@ -312,11 +319,20 @@ def run_ours(args, w, name, rank, world, peaks, quiet=False):
             torch.cuda.synchronize()
             hits.append((time.perf_counter() - t0) * 1e3)
         hit_ms = statistics.median(hits)
+    # host time to enqueue one warm call (no synchronisation)
+    torch.cuda.synchronize()
+    enq = []
+    for i in range(200):
+        t0 = time.perf_counter()
+        call(i)
+        enq.append((time.perf_counter() - t0) * 1e6)
+    torch.cuda.synchronize()
+    enqueue_us = statistics.median(enq)
     # timed region
     for i in range(args.warmup):
         mm.check(call(i))
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(args.steps)]
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
     sampler = ClockSampler(dev.index if dev.index is not None else 0)
     if world > 1:
         torch.distributed.barrier()
@@ -324,18 +340,19 @@ def run_ours(args, w, name, rank, world, peaks, quiet=False):
     sampler.start()
     time.sleep(0.3)
     launches0 = mm.mm_get_stats()["launches"]
+    ev0.record(stream)
     for i in range(args.steps):
-        ev[i][0].record(stream)
         call(i)
-        ev[i][1].record(stream)
+    ev1.record(stream)
     torch.cuda.synchronize()
     launches = mm.mm_get_stats()["launches"] - launches0
     if world > 1:
         torch.distributed.barrier()
     clocks = sampler.stop()
-    total_ms = ev[0][0].elapsed_time(ev[-1][1])
-    per_launch = [a.elapsed_time(b_) for a, b_ in ev]
-    kern_ms = statistics.mean(per_launch)
+    total_ms = ev0.elapsed_time(ev1)
+    # every warm step is one call of the tuned candidate: its mean device time
+    # per launch is the timed loop's device time over the steps
+    kern_ms = total_ms / args.steps
     if world > 1:
         t = torch.tensor([total_ms], device=dev)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
@@ -390,6 +407,7 @@ def run_ours(args, w, name, rank, world, peaks, quiet=False):
                    "parallelism": f"replicas{world}",
                    "l2": f"{R} rotating input sets of {set_bytes / 1e6:.1f} MB (> 2 x L2)"},
         "winner": winner, "cold_tune_ms": cold_ms, "cache_hit_ms": hit_ms,
+        "host_enqueue_us": enqueue_us,
         "gpu_launches": int(launches), "clocks": clocks, "roofline": roof,
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "steps": e2e_steps,
                 "h2d_bytes_per_step": int(A.buf.nbytes + B.buf.nbytes),
@@ -409,6 +427,7 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
     ap.add_argument("--report", action="store_true")
     ap.add_argument("--cpu-budget-s", type=float, default=15.0)
+    ap.add_argument("--only", default=None, help="with --report: comma-separated name filters")
     ap.add_argument("--candidate", default=None,
                     help="run this candidate directly (no tuning); for profiling")
     args = ap.parse_args()
@@ -428,6 +447,8 @@ def main():
         torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local))
     peaks = load_peaks()
     names = sorted(WORKLOADS) if args.report else [args.workload]
+    if args.only:
+        names = [n for n in names if any(o in n for o in args.only.split(","))]
     for name in names:
         wl = workload_shape(name)
         steps = args.steps

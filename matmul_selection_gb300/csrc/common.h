@@ -188,7 +188,7 @@ void for_each_device(void (*fn)(DeviceState &));
 
 // Scratch of at least `bytes` private to (device, stream, slot).  A new or
 // grown buffer is zero-filled (stream-ordered).
-enum ScratchSlot { SCRATCH_TICKETS = 0, SCRATCH_WORKSPACE = 1 };
+enum ScratchSlot { SCRATCH_TICKETS = 0, SCRATCH_WORKSPACE = 1, SCRATCH_REPACK = 2 };
 mm_status get_scratch(DeviceState &ds, cudaStream_t s, int slot, size_t bytes, void **out);
 
 // ---------------------------------------------------------------- candidates
@@ -231,6 +231,7 @@ mm_status launch_candidate(int index, const Problem &p, LaunchCtx &ctx);
 mm_status launch_naive(const Problem &p, cudaStream_t s);
 mm_status launch_l2_flush(void *buf, size_t bytes, cudaStream_t s);
 mm_status launch_empty(cudaStream_t s);
+mm_status launch_delay(unsigned long long ns, cudaStream_t s);
 mm_status launch_copy_probe(const void *src, void *dst, size_t bytes, cudaStream_t s);
 mm_status launch_compare(const void *x, const void *ref, int dtype, int64_t rows, int64_t cols,
                          int64_t ld, int64_t batch, int64_t bstride, double atol, double rtol,
@@ -240,6 +241,16 @@ bool gemv_supports(const Problem &p, const DeviceInfo &d, int cfg, std::string *
 mm_status launch_gemv(const Problem &p, LaunchCtx &ctx, int cfg);
 int gemv_config_count();
 const char *gemv_config_name(int cfg);
+
+bool gemv_fast_supports(const Problem &p, const DeviceInfo &d, int cfg, std::string *why);
+mm_status launch_gemv_fast(const Problem &p, LaunchCtx &ctx, int cfg);
+int gemv_fast_config_count();
+const char *gemv_fast_config_name(int cfg);
+
+bool repack_supports(const Problem &p, const DeviceInfo &d, int cfg, std::string *why);
+mm_status launch_repack(const Problem &p, LaunchCtx &ctx, int cfg);
+int repack_config_count();
+const char *repack_config_name(int cfg);
 
 bool tc_supports(const Problem &p, const DeviceInfo &d, int cfg, std::string *why);
 mm_status launch_tc(const Problem &p, LaunchCtx &ctx, int cfg);

@@ -1,0 +1,460 @@
+// Latency-lean GEMV candidates for small M.
+//
+// At M <= 8 the product is a single pass over B (33.5 MB for 4096 x 4096
+// bf16); on this part a bare 33.5 MB read already costs ~8 us per launch, so
+// these kernels are built to add as little as possible to it:
+//   * every thread issues its loads of B before anything else (A staging and
+//     all synchronisation happen while those loads are in flight);
+//   * A is staged with batched loads (all issued, then stored);
+//   * no second kernel and no serial tail.
+//
+//   gemv_n_cluster  B row-major [K][N].  A cluster of 8 CTAs shares one group
+//       of CW columns (256 bytes of every row); CTA rank s handles the K rows
+//       [s*KS, (s+1)*KS).  In a CTA, 16 lanes cover a row segment with 16-byte
+//       loads (2 rows per warp instruction, 32 rows per step).  Partials are
+//       summed in a fixed order: the two rows of a warp by shuffle, the 16 warps
+//       through shared memory, then the 8 CTAs through distributed shared
+//       memory, rank 0..7 in order, each rank finishing CW/8 of the columns.
+//   gemv_t_rows  B transposed [N][K].  One warp per output column (row of B)
+//       reading the whole row with 16-byte loads; the dot products end in an
+//       xor-shuffle reduction.  No cross-warp or cross-CTA combination.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <mutex>
+
+#include "../common.h"
+
+namespace mm {
+
+namespace {
+
+constexpr int kThreads = 512;
+constexpr int kWarps = kThreads / 32;
+constexpr int kCluster = 8;
+
+__device__ __forceinline__ float ld_any(const void *p, int64_t i, int t) {
+  if (t == MM_F32) return static_cast<const float *>(p)[i];
+  if (t == MM_BF16) return __bfloat162float(static_cast<const __nv_bfloat16 *>(p)[i]);
+  return __half2float(static_cast<const __half *>(p)[i]);
+}
+__device__ __forceinline__ void st_any(void *p, int64_t i, int t, float v) {
+  if (t == MM_F32)
+    static_cast<float *>(p)[i] = v;
+  else if (t == MM_BF16)
+    static_cast<__nv_bfloat16 *>(p)[i] = __float2bfloat16_rn(v);
+  else
+    static_cast<__half *>(p)[i] = __float2half_rn(v);
+}
+
+// 16 bytes of B -> VEC floats.
+template <int TB>
+__device__ __forceinline__ void unpack16(const uint4 &q, float *f) {
+  const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+  if constexpr (TB == MM_F32) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) f[i] = __uint_as_float(w[i]);
+  } else if constexpr (TB == MM_BF16) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      f[2 * i] = __uint_as_float(w[i] << 16);
+      f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float2 x = __half22float2(*reinterpret_cast<const __half2 *>(&w[i]));
+      f[2 * i] = x.x;
+      f[2 * i + 1] = x.y;
+    }
+  }
+}
+
+// 16-byte load of elements [e, e+VEC) of a row of length len (zeros past it).
+template <int TB>
+__device__ __forceinline__ uint4 load16(const char *row, int64_t e, int64_t len) {
+  constexpr int EB = TB == MM_F32 ? 4 : 2;
+  constexpr int VEC = 16 / EB;
+  if (e + VEC <= len) return __ldcs(reinterpret_cast<const uint4 *>(row + e * EB));
+  uint32_t w[4] = {0, 0, 0, 0};
+  if (e < len) {
+    if constexpr (EB == 4) {
+      for (int i = 0; i < 4; ++i)
+        if (e + i < len) w[i] = reinterpret_cast<const uint32_t *>(row)[e + i];
+    } else {
+      for (int i = 0; i < 8; ++i)
+        if (e + i < len) {
+          uint32_t h = reinterpret_cast<const uint16_t *>(row)[e + i];
+          w[i / 2] |= (i & 1) ? (h << 16) : h;
+        }
+    }
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+struct FastArgs {
+  const void *A;
+  int ta;
+  int64_t a_rs, a_cs, sA;
+  const char *B;
+  int64_t ldb, sB;
+  void *C;
+  int tc;
+  int64_t ldc, sC;
+  int M, N, K, batch;
+  int KS;  // gemv_n_cluster: rows per cluster rank
+};
+
+// Stage n_elems elements of A (index -> (m, k) by `map`) into smem as fp32,
+// loads batched 8 at a time so their latencies overlap.
+template <typename Map>
+__device__ __forceinline__ void stage_batched(const FastArgs &g, float *dst, int n_elems, Map map) {
+  for (int base = threadIdx.x; base < n_elems; base += kThreads * 8) {
+    float v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int e = base + u * kThreads;
+      int64_t off;
+      bool ok = e < n_elems && map(e, &off);
+      v[u] = ok ? ld_any(g.A, off, g.ta) : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int e = base + u * kThreads;
+      if (e < n_elems) dst[e] = v[u];
+    }
+  }
+}
+
+// ---------------------------------------------------------------- gemv_n_cluster
+template <int MT, int TB>
+__global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1) gemv_n_cluster_kernel(const FastArgs g) {
+  constexpr int EB = TB == MM_F32 ? 4 : 2;
+  constexpr int VEC = 16 / EB;
+  constexpr int CW = 256 / EB;          // columns per group: 256 bytes of a row
+  constexpr int LPR = CW / VEC;         // 16 lanes per row segment
+  constexpr int RPW = 32 / LPR;         // 2 rows per warp instruction
+  constexpr int STEP = kWarps * RPW;    // 32 rows per step
+  constexpr int U = 8;                  // loads in flight per lane
+  constexpr int CPR = CW / kCluster;    // columns each rank finishes
+  constexpr int APT = MT;               // A elements a thread preloads (slices of <= 512 rows)
+  extern __shared__ float fsm[];
+  float *As = fsm;                              // [KS][MT]
+  float *part = fsm + g.KS * MT;                // [warps][MT][CW], slot 0 ends as the CTA sum
+  const int grp = blockIdx.x, b = blockIdx.z;
+  uint32_t rank;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(rank));
+  const int k0 = (int)rank * g.KS;
+  const int kr = max(0, min(g.KS, g.K - k0));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int sub = lane / LPR, li = lane % LPR;
+  const int col = grp * CW + li * VEC;
+  const char *Bb = g.B + (int64_t)b * g.sB * EB;
+  // this thread's elements of A's slice: issued first, stored after B's loads
+  const int na = g.KS * MT;
+  float areg[APT];
+#pragma unroll
+  for (int u = 0; u < APT; ++u) {
+    const int e = threadIdx.x + u * kThreads;
+    const int kk = e / MT, m = e - kk * MT;
+    areg[u] = (e < na && m < g.M && kk < kr)
+                  ? ld_any(g.A, (int64_t)b * g.sA + (int64_t)m * g.a_rs + (int64_t)(k0 + kk) * g.a_cs,
+                           g.ta)
+                  : 0.f;
+  }
+  float acc[MT][VEC];
+#pragma unroll
+  for (int m = 0; m < MT; ++m)
+#pragma unroll
+    for (int j = 0; j < VEC; ++j) acc[m][j] = 0.f;
+  bool staged = false;
+  for (int r0 = warp * RPW + sub; r0 < g.KS; r0 += STEP * U) {
+    uint4 v[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int r = r0 + u * STEP;
+      v[u] = (r < kr) ? load16<TB>(Bb + (int64_t)(k0 + r) * g.ldb * EB, col, g.N)
+                      : make_uint4(0, 0, 0, 0);
+    }
+    if (!staged) {  // B's first loads are in flight; now publish A's slice
+#pragma unroll
+      for (int u = 0; u < APT; ++u) {
+        const int e = threadIdx.x + u * kThreads;
+        if (e < na) As[e] = areg[u];
+      }
+      for (int e = threadIdx.x + APT * kThreads; e < na; e += kThreads) {  // slices > 512 rows
+        const int kk = e / MT, m = e - kk * MT;
+        As[e] = (m < g.M && kk < kr) ? ld_any(g.A, (int64_t)b * g.sA + (int64_t)m * g.a_rs +
+                                                       (int64_t)(k0 + kk) * g.a_cs, g.ta)
+                                     : 0.f;
+      }
+      __syncthreads();
+      staged = true;
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int r = r0 + u * STEP;
+      if (r < kr) {
+        float bf[VEC];
+        unpack16<TB>(v[u], bf);
+        const float *a = As + r * MT;
+#pragma unroll
+        for (int m = 0; m < MT; ++m)
+#pragma unroll
+          for (int j = 0; j < VEC; ++j) acc[m][j] = fmaf(a[m], bf[j], acc[m][j]);
+      }
+    }
+  }
+  // rows of a warp: fixed-order xor shuffle over the RPW row lanes
+#pragma unroll
+  for (int m = 0; m < MT; ++m)
+#pragma unroll
+    for (int j = 0; j < VEC; ++j) {
+      float x = acc[m][j];
+#pragma unroll
+      for (int o = LPR; o < 32; o <<= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+      acc[m][j] = x;
+    }
+  if (sub == 0)
+#pragma unroll
+    for (int m = 0; m < MT; ++m)
+#pragma unroll
+      for (int j = 0; j < VEC; ++j) part[(warp * MT + m) * CW + li * VEC + j] = acc[m][j];
+  __syncthreads();
+  // the CTA's sum over warps 0..15 in order, into slot 0
+  float cta[2];
+  int ncta = 0;
+  for (int e = threadIdx.x; e < MT * CW; e += kThreads) {
+    float t = 0.f;
+    for (int w = 0; w < kWarps; ++w) t += part[w * MT * CW + e];
+    cta[ncta++] = t;
+  }
+  __syncthreads();
+  ncta = 0;
+  for (int e = threadIdx.x; e < MT * CW; e += kThreads) part[e] = cta[ncta++];
+  // all ranks' sums visible cluster-wide
+  asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+  const uint32_t part_addr = (uint32_t)__cvta_generic_to_shared(part);
+  for (int e = threadIdx.x; e < MT * CPR; e += kThreads) {
+    const int m = e / CPR, c = (int)rank * CPR + (e - m * CPR);
+    float t = 0.f;
+#pragma unroll
+    for (int q = 0; q < kCluster; ++q) {
+      uint32_t ra;
+      asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
+                   : "=r"(ra)
+                   : "r"(part_addr + (uint32_t)((m * CW + c) * 4)), "r"(q));
+      float x;
+      asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(x) : "r"(ra) : "memory");
+      t += x;
+    }
+    const int n = grp * CW + c;
+    if (m < g.M && n < g.N) st_any(g.C, (int64_t)b * g.sC + (int64_t)m * g.ldc + n, g.tc, t);
+  }
+  // keep this CTA's shared memory alive until every rank has read it
+  asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+
+// ---------------------------------------------------------------- gemv_t_rows
+template <int MT, int TB>
+__global__ void __launch_bounds__(kThreads, MT <= 2 ? 2 : 1) gemv_t_rows_kernel(const FastArgs g) {
+  constexpr int EB = TB == MM_F32 ? 4 : 2;
+  constexpr int VEC = 16 / EB;
+  constexpr int U = 8;
+  extern __shared__ float fsm[];
+  float *As = fsm;  // [MT][K]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int b = blockIdx.y;
+  const int n = blockIdx.x * kWarps + warp;
+  const char *row = g.B + ((int64_t)b * g.sB + (int64_t)min(n, g.N - 1) * g.ldb) * EB;
+  const bool valid = n < g.N;
+  float acc[MT];
+#pragma unroll
+  for (int m = 0; m < MT; ++m) acc[m] = 0.f;
+  bool staged = false;
+  for (int kb = 0; kb < g.K; kb += 32 * VEC * U) {
+    uint4 v[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int k = kb + (u * 32 + lane) * VEC;
+      v[u] = valid ? load16<TB>(row, k, g.K) : make_uint4(0, 0, 0, 0);
+    }
+    if (!staged) {
+      stage_batched(g, As, MT * g.K, [&](int e, int64_t *off) {
+        const int m = e / g.K, k = e - m * g.K;
+        if (m >= g.M) return false;
+        *off = (int64_t)b * g.sA + (int64_t)m * g.a_rs + (int64_t)k * g.a_cs;
+        return true;
+      });
+      __syncthreads();
+      staged = true;
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int k = kb + (u * 32 + lane) * VEC;
+      if (k < g.K) {
+        float bf[VEC];
+        unpack16<TB>(v[u], bf);
+#pragma unroll
+        for (int m = 0; m < MT; ++m) {
+          const float *a = As + (int64_t)m * g.K + k;
+          float t = acc[m];
+#pragma unroll
+          for (int j = 0; j < VEC; ++j)
+            if (k + j < g.K) t = fmaf(a[j], bf[j], t);
+          acc[m] = t;
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int m = 0; m < MT; ++m) {
+    float x = acc[m];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    if (lane == 0 && valid && m < g.M)
+      st_any(g.C, (int64_t)b * g.sC + (int64_t)m * g.ldc + n, g.tc, x);
+  }
+}
+
+// ---------------------------------------------------------------- host
+struct FastCfg {
+  const char *name;
+  bool b_trans;
+};
+const FastCfg kFastCfgs[] = {{"gemv_n_cluster", false}, {"gemv_t_rows", true}};
+
+int mt_of(int64_t M) { return M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : 8; }
+
+constexpr int kMaxM = 8;
+constexpr size_t kMaxSmem = 96 * 1024;
+
+size_t smem_n(int mt, int ks, int eb) {
+  return ((size_t)ks * mt + (size_t)kWarps * mt * (256 / eb)) * sizeof(float);
+}
+size_t smem_t(int mt, int64_t K) { return (size_t)mt * K * sizeof(float); }
+
+int rows_per_rank(int64_t K) {
+  int64_t ks = (K + kCluster - 1) / kCluster;
+  return (int)((ks + 31) / 32 * 32);
+}
+
+template <typename F>
+cudaError_t smem_attr(F kern, size_t smem) {
+  static std::mutex mu;
+  static std::map<const void *, size_t> have;
+  std::lock_guard<std::mutex> lk(mu);
+  size_t &h = have[reinterpret_cast<const void *>(kern)];
+  if (smem <= h || smem <= 48 * 1024) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e == cudaSuccess) h = smem;
+  return e;
+}
+
+template <int MT, int TB>
+mm_status launch_n(const FastArgs &g, int groups, size_t smem, cudaStream_t s) {
+  auto kern = gemv_n_cluster_kernel<MT, TB>;
+  cudaError_t e = smem_attr(kern, smem);
+  if (e != cudaSuccess) return cuda_error(e, "gemv_n_cluster smem attribute");
+  cudaLaunchConfig_t lc = {};
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = 1;
+  at[0].val.clusterDim.y = kCluster;
+  at[0].val.clusterDim.z = 1;
+  lc.gridDim = dim3((unsigned)groups, kCluster, (unsigned)g.batch);
+  lc.blockDim = dim3(kThreads);
+  lc.dynamicSmemBytes = smem;
+  lc.stream = s;
+  lc.attrs = at;
+  lc.numAttrs = 1;
+  e = cudaLaunchKernelEx(&lc, kern, g);
+  return e == cudaSuccess ? MM_OK : cuda_error(e, "gemv_n_cluster launch");
+}
+
+template <int MT, int TB>
+mm_status launch_t(const FastArgs &g, size_t smem, cudaStream_t s) {
+  auto kern = gemv_t_rows_kernel<MT, TB>;
+  cudaError_t e = smem_attr(kern, smem);
+  if (e != cudaSuccess) return cuda_error(e, "gemv_t_rows smem attribute");
+  dim3 grid((unsigned)((g.N + kWarps - 1) / kWarps), (unsigned)g.batch);
+  kern<<<grid, kThreads, smem, s>>>(g);
+  e = cudaGetLastError();
+  return e == cudaSuccess ? MM_OK : cuda_error(e, "gemv_t_rows launch");
+}
+
+template <int TB>
+mm_status launch_tb(bool bt, int mt, const FastArgs &g, int groups, size_t smem, cudaStream_t s) {
+  switch (mt) {
+  case 1: return bt ? launch_t<1, TB>(g, smem, s) : launch_n<1, TB>(g, groups, smem, s);
+  case 2: return bt ? launch_t<2, TB>(g, smem, s) : launch_n<2, TB>(g, groups, smem, s);
+  case 4: return bt ? launch_t<4, TB>(g, smem, s) : launch_n<4, TB>(g, groups, smem, s);
+  default: return bt ? launch_t<8, TB>(g, smem, s) : launch_n<8, TB>(g, groups, smem, s);
+  }
+}
+
+}  // namespace
+
+int gemv_fast_config_count() { return (int)(sizeof kFastCfgs / sizeof kFastCfgs[0]); }
+const char *gemv_fast_config_name(int cfg) { return kFastCfgs[cfg].name; }
+
+bool gemv_fast_supports(const Problem &p, const DeviceInfo &d, int cfg, std::string *why) {
+  auto no = [&](const char *w) {
+    if (why) *why = w;
+    return false;
+  };
+  const FastCfg &c = kFastCfgs[cfg];
+  if (d.cc_major != 10) return no("needs an sm_10x device");
+  if (p.bt != c.b_trans) return no("B layout does not match this variant");
+  if (p.M < 1 || p.M > kMaxM) return no("M outside [1, 8]");
+  if (p.K < 1 || p.N < 1) return no("empty problem");
+  if (p.N >= (1LL << 30) || p.K >= (1LL << 30) || p.batch > 65535) return no("too large");
+  const int eb = dtype_bytes(p.tb);
+  if ((uintptr_t)p.B % 16) return no("B not 16-byte aligned");
+  if ((p.ldb * eb) % 16) return no("ldb not a multiple of 16 bytes");
+  if (p.batch > 1 && (p.sB * eb) % 16) return no("B batch stride not a multiple of 16 bytes");
+  const int mt = mt_of(p.M);
+  size_t smem = c.b_trans ? smem_t(mt, p.K) : smem_n(mt, rows_per_rank(p.K), eb);
+  if (smem > kMaxSmem || (int64_t)smem > d.smem_optin) return no("A slice too large for shared memory");
+  return true;
+}
+
+mm_status launch_gemv_fast(const Problem &p, LaunchCtx &ctx, int cfg) {
+  std::string why;
+  if (!gemv_fast_supports(p, ctx.dev->info, cfg, &why))
+    return set_error(MM_ERR_UNSUPPORTED, "%s: %s", kFastCfgs[cfg].name, why.c_str());
+  const FastCfg &c = kFastCfgs[cfg];
+  const int eb = dtype_bytes(p.tb), mt = mt_of(p.M);
+  FastArgs g;
+  std::memset(&g, 0, sizeof g);
+  g.A = p.A;
+  g.ta = p.ta;
+  g.a_rs = p.at ? 1 : p.lda;
+  g.a_cs = p.at ? p.lda : 1;
+  g.sA = p.sA;
+  g.B = static_cast<const char *>(p.B);
+  g.ldb = p.ldb;
+  g.sB = p.sB;
+  g.C = p.C;
+  g.tc = p.tc;
+  g.ldc = p.ldc;
+  g.sC = p.sC;
+  g.M = (int)p.M;
+  g.N = (int)p.N;
+  g.K = (int)p.K;
+  g.batch = (int)p.batch;
+  int groups = 0;
+  size_t smem;
+  if (!c.b_trans) {
+    g.KS = rows_per_rank(p.K);
+    groups = (int)((p.N + 256 / eb - 1) / (256 / eb));
+    smem = smem_n(mt, g.KS, eb);
+  } else {
+    smem = smem_t(mt, p.K);
+  }
+  if (p.tb == MM_BF16) return launch_tb<MM_BF16>(c.b_trans, mt, g, groups, smem, ctx.stream);
+  if (p.tb == MM_F16) return launch_tb<MM_F16>(c.b_trans, mt, g, groups, smem, ctx.stream);
+  return launch_tb<MM_F32>(c.b_trans, mt, g, groups, smem, ctx.stream);
+}
+
+}  // namespace mm

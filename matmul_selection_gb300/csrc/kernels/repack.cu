@@ -1,0 +1,180 @@
+// Tensor-core candidates for operands that TMA cannot read in place.
+//
+// The key's stride factor records when a leading dimension (or base) is not
+// 16-byte aligned (e.g. a bf16 lda of 4100: 8200-byte rows, stride factor
+// 3); TMA-fed kernels cannot describe such an operand (burn "autotune" page:
+// the stride alignment decides whether TMA-style kernels can run).  These
+// candidates copy each misaligned operand once per call into library scratch
+// with its leading dimension rounded up to 16 bytes, then run a tensor-core
+// configuration on the copy.  The copy moves each misaligned operand once
+// more through HBM; for the large shapes that need it this is a few percent
+// of the product's time, against the naive kernel otherwise left.
+#include <type_traits>
+
+#include "../common.h"
+
+namespace mm {
+
+namespace {
+
+// Copy `rows` rows of `row_bytes` from a strided source to a strided
+// destination, G bytes per thread step (G divides every address and size).
+template <int G>
+__global__ void repack_kernel(const char *__restrict__ src, char *__restrict__ dst, int64_t rows,
+                              int64_t row_bytes, int64_t src_ld, int64_t dst_ld, int64_t batch,
+                              int64_t src_bs, int64_t dst_bs) {
+  using T = typename std::conditional<
+      G == 16, uint4,
+      typename std::conditional<G == 8, uint2,
+                                typename std::conditional<G == 4, uint32_t, uint16_t>::type>::type>::type;
+  const int64_t units = row_bytes / G;
+  const int64_t total = batch * rows * units;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t u = i % units, r = (i / units) % rows, b = i / (units * rows);
+    const T v = *reinterpret_cast<const T *>(src + b * src_bs + r * src_ld + u * G);
+    *reinterpret_cast<T *>(dst + b * dst_bs + r * dst_ld + u * G) = v;
+  }
+}
+
+struct RepackCfg {
+  const char *name;
+  const char *inner;  // tensor-core configuration run on the copies
+};
+const RepackCfg kRepackCfgs[] = {
+    {"tc2_repack_256x256", "tc2_256x256_s6"},
+    {"tc_repack_128x128", "tc_128x128_s6"},
+    {"tc_repack_128x64", "tc_128x64_s8"},
+};
+
+struct Plan {
+  bool a, b;               // which operands are copied
+  int64_t lda2, ldb2;      // leading dimensions of the copies (elements)
+  int64_t sA2, sB2;        // batch strides of the copies (elements)
+  size_t bytes_a, bytes_b; // scratch bytes for each copy
+  Problem q;               // the problem on the copies (pointers filled at launch)
+};
+
+bool aligned16(const void *p, int64_t ld, int64_t bs, int64_t batch, int es) {
+  return (uintptr_t)p % 16 == 0 && (ld * es) % 16 == 0 && (batch <= 1 || (bs * es) % 16 == 0);
+}
+
+// Rows / row length of an operand as stored.
+void storage_shape(int64_t rows_logical, int64_t cols_logical, bool trans, int64_t *rows,
+                   int64_t *row_elems) {
+  *rows = trans ? cols_logical : rows_logical;
+  *row_elems = trans ? rows_logical : cols_logical;
+}
+
+Plan make_plan_for(const Problem &p) {
+  Plan pl;
+  const int es = dtype_bytes(p.ta);
+  const int64_t round = 16 / es;
+  pl.a = !aligned16(p.A, p.lda, p.sA, p.batch, es);
+  pl.b = !aligned16(p.B, p.ldb, p.sB, p.batch, es);
+  int64_t ra, ea, rb, eb;
+  storage_shape(p.M, p.K, p.at, &ra, &ea);
+  storage_shape(p.K, p.N, p.bt, &rb, &eb);
+  pl.lda2 = (ea + round - 1) / round * round;
+  pl.ldb2 = (eb + round - 1) / round * round;
+  pl.sA2 = ra * pl.lda2;
+  pl.sB2 = rb * pl.ldb2;
+  pl.bytes_a = pl.a ? (size_t)(p.batch * pl.sA2 * es + 256) : 0;
+  pl.bytes_b = pl.b ? (size_t)(p.batch * pl.sB2 * es + 256) : 0;
+  pl.q = p;
+  if (pl.a) {
+    pl.q.lda = pl.lda2;
+    pl.q.sA = pl.sA2;
+  }
+  if (pl.b) {
+    pl.q.ldb = pl.ldb2;
+    pl.q.sB = pl.sB2;
+  }
+  return pl;
+}
+
+int inner_index(int cfg) { return tc_config_index(kRepackCfgs[cfg].inner); }
+
+mm_status repack(const void *src, void *dst, int64_t rows, int64_t row_bytes, int64_t src_ld,
+                 int64_t dst_ld, int64_t batch, int64_t src_bs, int64_t dst_bs, int sms,
+                 cudaStream_t s) {
+  auto ok = [&](int g) {
+    return (uintptr_t)src % g == 0 && (uintptr_t)dst % g == 0 && row_bytes % g == 0 &&
+           src_ld % g == 0 && dst_ld % g == 0 && (batch <= 1 || (src_bs % g == 0 && dst_bs % g == 0));
+  };
+  const int64_t total_bytes = batch * rows * row_bytes;
+  int g = ok(16) ? 16 : ok(8) ? 8 : ok(4) ? 4 : 2;
+  int64_t units = total_bytes / g;
+  int blocks = (int)std::min<int64_t>((units + 255) / 256, (int64_t)sms * 16);
+  if (blocks < 1) blocks = 1;
+  const char *sp = static_cast<const char *>(src);
+  char *dp = static_cast<char *>(dst);
+  switch (g) {
+  case 16: repack_kernel<16><<<blocks, 256, 0, s>>>(sp, dp, rows, row_bytes, src_ld, dst_ld, batch, src_bs, dst_bs); break;
+  case 8: repack_kernel<8><<<blocks, 256, 0, s>>>(sp, dp, rows, row_bytes, src_ld, dst_ld, batch, src_bs, dst_bs); break;
+  case 4: repack_kernel<4><<<blocks, 256, 0, s>>>(sp, dp, rows, row_bytes, src_ld, dst_ld, batch, src_bs, dst_bs); break;
+  default: repack_kernel<2><<<blocks, 256, 0, s>>>(sp, dp, rows, row_bytes, src_ld, dst_ld, batch, src_bs, dst_bs); break;
+  }
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? MM_OK : cuda_error(e, "repack_kernel launch");
+}
+
+}  // namespace
+
+int repack_config_count() { return (int)(sizeof kRepackCfgs / sizeof kRepackCfgs[0]); }
+const char *repack_config_name(int cfg) { return kRepackCfgs[cfg].name; }
+
+bool repack_supports(const Problem &p, const DeviceInfo &d, int cfg, std::string *why) {
+  auto no = [&](const char *w) {
+    if (why) *why = w;
+    return false;
+  };
+  if (p.ta != p.tb) return no("A and B must have the same type");
+  if (p.M < 1 || p.N < 1 || p.K < 1) return no("empty problem");
+  const int es = dtype_bytes(p.ta);
+  if (((uintptr_t)p.A | (uintptr_t)p.B) % es) return no("operands not element-aligned");
+  Plan pl = make_plan_for(p);
+  if (!pl.a && !pl.b) return no("both operands TMA-aligned: the plain configuration applies");
+  const int inner = inner_index(cfg);
+  if (inner < 0) return no("inner configuration missing");
+  // the inner configuration must accept the aligned copies
+  Problem q = pl.q;
+  static char aligned_dummy[256] __attribute__((aligned(256)));
+  if (pl.a) q.A = aligned_dummy;
+  if (pl.b) q.B = aligned_dummy;
+  return tc_supports(q, d, inner, why);
+}
+
+mm_status launch_repack(const Problem &p, LaunchCtx &ctx, int cfg) {
+  std::string why;
+  if (!repack_supports(p, ctx.dev->info, cfg, &why))
+    return set_error(MM_ERR_UNSUPPORTED, "%s: %s", kRepackCfgs[cfg].name, why.c_str());
+  Plan pl = make_plan_for(p);
+  const int es = dtype_bytes(p.ta);
+  void *scr = nullptr;
+  mm_status st = get_scratch(*ctx.dev, ctx.stream, SCRATCH_REPACK, pl.bytes_a + pl.bytes_b + 512, &scr);
+  if (st != MM_OK) return st;
+  char *base = reinterpret_cast<char *>(((uintptr_t)scr + 255) & ~(uintptr_t)255);
+  Problem q = pl.q;
+  const int sms = ctx.dev->info.sms;
+  if (pl.a) {
+    int64_t rows, row_elems;
+    storage_shape(p.M, p.K, p.at, &rows, &row_elems);
+    st = repack(p.A, base, rows, row_elems * es, p.lda * es, pl.lda2 * es, p.batch, p.sA * es,
+                pl.sA2 * es, sms, ctx.stream);
+    if (st != MM_OK) return st;
+    q.A = base;
+    base += (pl.bytes_a + 255) & ~(size_t)255;
+  }
+  if (pl.b) {
+    int64_t rows, row_elems;
+    storage_shape(p.K, p.N, p.bt, &rows, &row_elems);
+    st = repack(p.B, base, rows, row_elems * es, p.ldb * es, pl.ldb2 * es, p.batch, p.sB * es,
+                pl.sB2 * es, sms, ctx.stream);
+    if (st != MM_OK) return st;
+    q.B = base;
+  }
+  return launch_tc(q, ctx, inner_index(cfg));
+}
+
+}  // namespace mm

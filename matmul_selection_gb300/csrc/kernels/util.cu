@@ -31,6 +31,18 @@ __global__ void copy_kernel(const uint4 *__restrict__ src, uint4 *__restrict__ d
   for (; i < n16; i += stride) dst[i] = src[i];
 }
 
+// Occupies the stream for about `ns` nanoseconds (one thread, bounded by
+// %globaltimer), so that work enqueued behind it meanwhile runs back to back.
+__global__ void delay_kernel(unsigned long long ns) {
+  unsigned long long t0;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
+  unsigned long long t = t0;
+  while (t - t0 < ns) {
+    __nanosleep(1000);
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  }
+}
+
 __device__ __forceinline__ float ld_any(const void *p, int64_t i, int t) {
   if (t == MM_F32) return static_cast<const float *>(p)[i];
   if (t == MM_BF16) return __bfloat162float(static_cast<const __nv_bfloat16 *>(p)[i]);
@@ -57,6 +69,13 @@ mm_status launch_empty(cudaStream_t s) {
   empty_kernel<<<1, 32, 0, s>>>(nullptr);
   cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? MM_OK : cuda_error(e, "empty_kernel launch");
+}
+
+mm_status launch_delay(unsigned long long ns, cudaStream_t s) {
+  if (ns > 10000000ull) ns = 10000000ull;  // never more than 10 ms
+  delay_kernel<<<1, 1, 0, s>>>(ns);
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? MM_OK : cuda_error(e, "delay_kernel launch");
 }
 
 mm_status launch_l2_flush(void *buf, size_t bytes, cudaStream_t s) {

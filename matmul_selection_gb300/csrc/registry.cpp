@@ -35,6 +35,8 @@ int prio_tc(const KeyPod &k, const Problem &, const DeviceInfo &d, int cfg) {
   return PRIORITY_MIN;
 }
 
+int prio_repack(const KeyPod &, const Problem &, const DeviceInfo &, int) { return PRIORITY_HIGH; }
+
 bool naive_supports(const Problem &, const DeviceInfo &, int, std::string *) { return true; }
 mm_status naive_launch(const Problem &p, LaunchCtx &ctx, int) { return launch_naive(p, ctx.stream); }
 
@@ -43,8 +45,14 @@ std::vector<Candidate> build_registry() {
   r.push_back({"naive", GROUP_NAIVE, 0, prio_naive, naive_supports, naive_launch});
   for (int i = 0; i < gemv_config_count(); ++i)
     r.push_back({gemv_config_name(i), GROUP_GEMV, i, prio_gemv, gemv_supports, launch_gemv});
+  for (int i = 0; i < gemv_fast_config_count(); ++i)
+    r.push_back({gemv_fast_config_name(i), GROUP_GEMV, i, prio_gemv, gemv_fast_supports,
+                 launch_gemv_fast});
   for (int i = 0; i < tc_config_count(); ++i)
     r.push_back({tc_config_name(i), GROUP_TENSOR, i, prio_tc, tc_supports, launch_tc});
+  for (int i = 0; i < repack_config_count(); ++i)
+    r.push_back({repack_config_name(i), GROUP_TENSOR, i, prio_repack, repack_supports,
+                 launch_repack});
   return r;
 }
 

@@ -15,6 +15,9 @@
 //   * a candidate with 2 samples inside the roofline time limit short-circuits
 //     the round: no further candidate of that round is measured;
 //   * the fastest MEDIAN wins; ties go to the lower candidate index.
+// Each chunk of timed iterations is enqueued behind a short delay kernel so
+// the iterations run back to back on the device; the events then time the
+// kernels rather than the host's launch latency.
 // Every timed iteration runs on its own rotating copy of the inputs and its
 // own private output (TunableOp's rotating buffer; the page's out.copy()), so
 // the user's output is never written by tuning and repeated runs do not
@@ -232,6 +235,9 @@ CandResult bench_candidate(int idx, BenchEnv &env, double best_ms) {
   while (true) {
     int chunk = first ? std::min(3, max_it) : std::min(10, max_it - n);
     if (chunk <= 0) break;
+    // hold the stream while the chunk is enqueued, so its iterations run back
+    // to back and the events time the device, not the host's launch latency
+    launch_delay(40000ull * (unsigned long long)chunk, ds.tune_stream);
     for (int i = 0; i < chunk; ++i) {
       const Problem &q = env.rot->sets[(n + i) % R];
       if (env.opts.l2_flush && ds.flush_buf.ptr) launch_l2_flush(ds.flush_buf.ptr, ds.flush_buf.bytes, ds.tune_stream);

@@ -98,6 +98,11 @@ def test_every_candidate_runs_somewhere():
         "naive": Case(33, 17, 9, dist="int4"),
         "gemv_n": Case(4, 256, 512, layout="NN", dist="int4"),
         "gemv_t": Case(4, 256, 512, layout="NT", dist="int4"),
+        "gemv_n_cluster": Case(4, 1000, 520, layout="NN", dist="int4"),
+        "gemv_t_rows": Case(3, 300, 1000, layout="NT", dist="int4"),
+        "tc2_repack_256x256": Case(300, 264, 200, layout="NN", dist="int4", pad=(4, 0, 0)),
+        "tc_repack_128x128": Case(300, 264, 200, layout="TN", dist="int4", pad=(3, 0, 0)),
+        "tc_repack_128x64": Case(130, 72, 136, layout="NT", dist="int4", pad=(0, 5, 0)),
     }
     for i, n in enumerate(NAMES):
         c = home.get(n) or Case(256, 256, 256, layout="NN", dist="int4")
@@ -155,7 +160,7 @@ def test_gemv_full_size_exact(M, layout):
         if run(i, c) == mm.MM_OK:
             c.check(exact=True)
             ran += 1
-    assert ran == 1
+    assert ran >= 1
 
 
 @pytest.mark.parametrize("M", [1, 8, 16])
