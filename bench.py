@@ -42,6 +42,10 @@ BF16, F16, F32 = synth.BF16, synth.F16, synth.F32
 # name -> (M, N, K, layout, (dtA, dtB, dtC), distA, distB, lda_pad, batch, seed)
 WORKLOADS = {
     "square_4096_bf16": (4096, 4096, 4096, "NN", (BF16, BF16, BF16), "normal", "normal", 0, 1, 1002),
+    "square_4096_bf16_nt": (4096, 4096, 4096, "NT", (BF16, BF16, BF16), "normal", "normal", 0, 1, 1002),
+    "square_4096_bf16_tn": (4096, 4096, 4096, "TN", (BF16, BF16, BF16), "normal", "normal", 0, 1, 1002),
+    "square_4096_bf16_tt": (4096, 4096, 4096, "TT", (BF16, BF16, BF16), "normal", "normal", 0, 1, 1002),
+    "square_8192_bf16": (8192, 8192, 8192, "NN", (BF16, BF16, BF16), "normal", "normal", 0, 1, 1002),
     "small_256_bf16": (256, 256, 256, "NN", (BF16, BF16, F32), "u11", "u11", 0, 1, 1000),
     "gemv_m1_4096_bf16": (1, 4096, 4096, "NN", (BF16, BF16, BF16), "normal", "normal:0.02", 0, 1, 1001),
     "gemv_m8_4096_bf16": (8, 4096, 4096, "NN", (BF16, BF16, BF16), "normal", "normal:0.02", 0, 1, 1001),
@@ -358,6 +362,25 @@ def run_ours(args, w, name, rank, world, peaks, quiet=False):
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         total_ms = float(t.item())
     value = flops * args.steps * world / (total_ms * 1e-3) / 1e12
+    # context only: the vendor library on the same shape and rotating inputs
+    cublas_tflops = None
+    if args.cublas and batch == 1 and not w["pad"] and dt[0] == dt[1] and dt[0] != F32:
+        tdt = {BF16: torch.bfloat16, F16: torch.float16}[dt[0]]
+        tA = [x[0].view(tdt).view(M, K) if w["layout"][0] == "N" else x[0].view(tdt).view(K, M).t()
+              for x in sets]
+        tB = [x[1].view(tdt).view(K, N) if w["layout"][1] == "N" else x[1].view(tdt).view(N, K).t()
+              for x in sets]
+        for i in range(5):
+            torch.matmul(tA[i % R], tB[i % R])
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        nrep = min(args.steps, 500)
+        for i in range(nrep):
+            torch.matmul(tA[i % R], tB[i % R])
+        e1.record(stream)
+        torch.cuda.synchronize()
+        cublas_tflops = flops * nrep / (e0.elapsed_time(e1) * 1e-3) / 1e12
     # end to end from pinned host buffers through the host entry point
     e2e_steps = max(1, min(args.steps, 50))
     pA = torch.empty(A.buf.nbytes, dtype=torch.uint8, pin_memory=True)
@@ -408,6 +431,7 @@ def run_ours(args, w, name, rank, world, peaks, quiet=False):
                    "l2": f"{R} rotating input sets of {set_bytes / 1e6:.1f} MB (> 2 x L2)"},
         "winner": winner, "cold_tune_ms": cold_ms, "cache_hit_ms": hit_ms,
         "host_enqueue_us": enqueue_us,
+        "context_cublas_tflops": cublas_tflops,
         "gpu_launches": int(launches), "clocks": clocks, "roofline": roof,
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "steps": e2e_steps,
                 "h2d_bytes_per_step": int(A.buf.nbytes + B.buf.nbytes),
@@ -427,6 +451,8 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
     ap.add_argument("--report", action="store_true")
     ap.add_argument("--cpu-budget-s", type=float, default=15.0)
+    ap.add_argument("--cublas", action="store_true",
+                    help="also time torch.matmul on the same shape (context, not a target)")
     ap.add_argument("--only", default=None, help="with --report: comma-separated name filters")
     ap.add_argument("--candidate", default=None,
                     help="run this candidate directly (no tuning); for profiling")

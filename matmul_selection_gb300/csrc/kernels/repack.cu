@@ -42,7 +42,7 @@ struct RepackCfg {
   const char *inner;  // tensor-core configuration run on the copies
 };
 const RepackCfg kRepackCfgs[] = {
-    {"tc2_repack_256x256", "tc2_256x256_s6"},
+    {"tc2_repack_256x256", "tc2_256x256_s7"},
     {"tc_repack_128x128", "tc_128x128_s6"},
     {"tc_repack_128x64", "tc_128x64_s8"},
 };

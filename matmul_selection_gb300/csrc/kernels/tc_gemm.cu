@@ -61,6 +61,10 @@ struct TcParams {
   uint32_t a_box_stride, b_box_stride;  // bytes between the TMA boxes of one stage (MN-major)
   int a_boxes, b_boxes, a_mn, b_mn;
   uint64_t timeout_ns;
+  // 2-SM kernel: units [0, full_units) are whole tiles; the remaining tiles
+  // of the last partial wave are split along N into two half-width units
+  int full_units;
+  uint32_t idesc_half;  // instruction descriptor for a half-width unit
 };
 
 // ---------------------------------------------------------------- PTX wrappers
@@ -572,17 +576,34 @@ __device__ __forceinline__ void umma_commit_pair_local(uint32_t bar) {
                : "memory");
 }
 
-constexpr uint32_t kPairSlack = 16384;  // shared memory after the ring (over-read guard)
+constexpr uint32_t kPairSlack = 0;  // shared memory reserved after the ring
+
+// Tile geometry of a 2-SM work unit: row tile, first column, batch, width.
+__device__ __forceinline__ void pair_unit(const TcParams &p, int u, int bn, int &tm, int &n0,
+                                          int &b, int &nw) {
+  int t = u, half = -1;
+  if (u >= p.full_units) {
+    const int v = u - p.full_units;
+    t = p.full_units + (v >> 1);
+    half = v & 1;
+  }
+  tm = t % p.tiles_m;
+  const int r = t / p.tiles_m;
+  const int tn = r % p.tiles_n;
+  b = r / p.tiles_n;
+  n0 = tn * bn + (half > 0 ? bn / 2 : 0);
+  nw = half < 0 ? bn : bn / 2;
+}
 
 template <int BN, int STAGES, int ES>
 __global__ void __launch_bounds__(kTcThreads, 1)
     tc2_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
-                    const __grid_constant__ CUtensorMap tmB, const TcParams p) {
+                    const __grid_constant__ CUtensorMap tmB,
+                    const __grid_constant__ CUtensorMap tmBh, const TcParams p) {
   constexpr int BNH = BN / 2;                 // B columns held by each CTA
   constexpr uint32_t A_BYTES = BM * 128;
   constexpr uint32_t B_BYTES = BNH * 128;
   constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
-  constexpr uint32_t PAIR_TX = 2 * STAGE_BYTES;
   constexpr int BK = 128 / ES;
   constexpr int UMMA_K = 32 / ES;
   constexpr int KSTEPS = BK / UMMA_K;
@@ -623,6 +644,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&tmA);
     prefetch_tmap(&tmB);
+    prefetch_tmap(&tmBh);
   }
   if (warp == 1) {
     tmem_alloc_pair(smem_u32(tmem_slot), TMEM_COLS);
@@ -642,10 +664,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       uint32_t phase = 0;
       bool ok = true;
       for (int u = cid; u < p.total_units && ok; u += ncl) {
-        int tm, tn, b, sp;
-        decode_unit(p, u, tm, tn, b, sp);
+        int tm, t0, b, nw;
+        pair_unit(p, u, BN, tm, t0, b, nw);
+        const int nh = nw / 2;  // B columns this CTA loads for the unit
         const int m0 = tm * PAIR_M + (int)rank * BM;
-        const int n0 = tn * BN + (int)rank * BNH;
+        const int n0 = t0 + (int)rank * nh;
+        const uint32_t tx = 2 * (A_BYTES + (uint32_t)nh * 128);
         for (int kb = 0; kb < p.num_kb; ++kb) {
           if (!wait_bounded(empty0 + 8 * stage, phase ^ 1, abort_flag, p.err, kErrProducer,
                             p.timeout_ns)) {
@@ -655,7 +679,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           const uint32_t lfb = leader_full0 + 8 * stage;
           const uint32_t sa = smem_u32(smem + stage * STAGE_BYTES);
           const uint32_t sb = sa + A_BYTES;
-          if (leader) mbar_expect_tx(full0 + 8 * stage, PAIR_TX);
+          if (leader) mbar_expect_tx(full0 + 8 * stage, tx);
           if (!p.a_mn) {
             tma_load_3d_pair(sa, &tmA, lfb, kb * BK, m0, b);
           } else {
@@ -663,9 +687,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
               tma_load_3d_pair(sa + j * p.a_box_stride, &tmA, lfb, m0 + j * ATOM, kb * BK, b);
           }
           if (!p.b_mn) {
-            tma_load_3d_pair(sb, &tmB, lfb, kb * BK, n0, b);
+            tma_load_3d_pair(sb, nw == BN ? &tmB : &tmBh, lfb, kb * BK, n0, b);
           } else {
-            for (int j = 0; j < p.b_boxes; ++j)
+            for (int j = 0; j < nh / ATOM; ++j)
               tma_load_3d_pair(sb + j * p.b_box_stride, &tmB, lfb, n0 + j * ATOM, kb * BK, b);
           }
           if (++stage == STAGES) {
@@ -692,6 +716,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       uint32_t acc_phase = 0;
       bool ok = true;
       for (int u = cid; u < p.total_units && ok; u += ncl) {
+        int tm_, t0_, b_, nw;
+        pair_unit(p, u, BN, tm_, t0_, b_, nw);
+        const uint32_t idesc = nw == BN ? p.idesc : p.idesc_half;
         if (!wait_bounded(tempty0 + 8 * acc, acc_phase ^ 1, abort_flag, p.err, kErrMma,
                           p.timeout_ns))
           break;
@@ -710,7 +737,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
           for (int kk = 0; kk < KSTEPS; ++kk)
             umma_pair<ES>(d_tmem, adesc + (uint64_t)(kk * p.a_kstep),
-                          bdesc + (uint64_t)(kk * p.b_kstep), p.idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+                          bdesc + (uint64_t)(kk * p.b_kstep), idesc, (kb > 0 || kk > 0) ? 1u : 0u);
           umma_commit_pair_both(empty0 + 8 * stage);
           if (++stage == STAGES) {
             stage = 0;
@@ -734,8 +761,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int u = cid; u < p.total_units; u += ncl) {
-      int tm, tn, b, sp;
-      decode_unit(p, u, tm, tn, b, sp);
+      int tm, n0, b, nw;
+      pair_unit(p, u, BN, tm, n0, b, nw);
       int ok = 1;
       if (lane == 0)
         ok = wait_bounded(tfull0 + 8 * acc, acc_phase, abort_flag, p.err, kErrEpilogue,
@@ -746,11 +773,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const int row = tm * PAIR_M + (int)rank * BM + q * 32 + lane;
       const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
 #pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
+      for (int c = 0; c < nw / 32; ++c) {
         uint32_t r[32];
         tmem_ld_32cols(tbase + (uint32_t)(c * 32), r);
         tmem_ld_wait();
-        store_chunk(p, b, 0, row, tn * BN + c * 32, r);
+        store_chunk(p, b, 0, row, n0 + c * 32, r);
       }
       tc_fence_before();
       __syncwarp();
@@ -804,7 +831,7 @@ const TcCfg kCfgs[] = {
     {"tc_128x64_s8", 64, 8, false, false},
     {"tc_splitk_128x128_s6", 128, 6, true, false},
     {"tc_splitk_128x64_s8", 64, 8, true, false},
-    {"tc2_256x256_s6", 256, 6, false, true},
+    {"tc2_256x256_s7", 256, 7, false, true},
     {"tc2_256x128_s8", 128, 8, false, true},
 };
 
@@ -883,47 +910,67 @@ mm_status launch_kernel(const CUtensorMap &ma, const CUtensorMap &mb, const TcPa
 }
 
 template <int BN, int STAGES, int ES>
-mm_status launch_pair_kernel(const CUtensorMap &ma, const CUtensorMap &mb, const TcParams &tp,
-                             int64_t units, cudaStream_t s) {
-  static std::once_flag once;
-  static cudaError_t attr_err = cudaSuccess;
-  static int max_clusters = 0;
-  const TcCfg cfg_shape{"", BN, STAGES, false, true};
-  const size_t smem = smem_bytes_cfg(cfg_shape);
-  auto kern = tc2_gemm_kernel<BN, STAGES, ES>;
-  cudaLaunchConfig_t lc = {};
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  lc.blockDim = dim3(kTcThreads);
-  lc.dynamicSmemBytes = smem;
-  lc.stream = s;
-  lc.attrs = attr;
-  lc.numAttrs = 1;
-  std::call_once(once, [&] {
-    attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (attr_err == cudaSuccess) {
-      cudaLaunchConfig_t q = lc;
-      q.gridDim = dim3(2);
-      attr_err = cudaOccupancyMaxActiveClusters(&max_clusters, kern, &q);
-    }
-  });
-  if (attr_err != cudaSuccess) return cuda_error(attr_err, "tc2 kernel set-up");
-  if (max_clusters < 1) return set_error(MM_ERR_UNSUPPORTED, "no CTA pair fits on this device");
-  const int64_t clusters = std::min<int64_t>(units, max_clusters);
-  lc.gridDim = dim3((unsigned)(2 * clusters));
-  cudaError_t e = cudaLaunchKernelEx(&lc, kern, ma, mb, tp);
-  if (e != cudaSuccess) return cuda_error(e, "tc2_gemm_kernel launch");
-  return MM_OK;
+struct PairKernel {
+  static cudaLaunchConfig_t config(size_t smem, cudaStream_t s, cudaLaunchAttribute *attr) {
+    cudaLaunchConfig_t lc = {};
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    lc.blockDim = dim3(kTcThreads);
+    lc.dynamicSmemBytes = smem;
+    lc.stream = s;
+    lc.attrs = attr;
+    lc.numAttrs = 1;
+    return lc;
+  }
+  static size_t smem() {
+    const TcCfg shape{"", BN, STAGES, false, true};
+    return smem_bytes_cfg(shape);
+  }
+  // Set-up once: shared-memory attribute and how many pairs fit at once.
+  static mm_status capacity(int *max_clusters) {
+    static std::once_flag once;
+    static cudaError_t err = cudaSuccess;
+    static int clusters = 0;
+    std::call_once(once, [] {
+      auto kern = tc2_gemm_kernel<BN, STAGES, ES>;
+      err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem());
+      if (err == cudaSuccess) {
+        cudaLaunchAttribute attr[1];
+        cudaLaunchConfig_t q = config(smem(), nullptr, attr);
+        q.gridDim = dim3(2);
+        err = cudaOccupancyMaxActiveClusters(&clusters, kern, &q);
+      }
+    });
+    if (err != cudaSuccess) return cuda_error(err, "tc2 kernel set-up");
+    if (clusters < 1) return set_error(MM_ERR_UNSUPPORTED, "no CTA pair fits on this device");
+    *max_clusters = clusters;
+    return MM_OK;
+  }
+  static mm_status launch(const CUtensorMap &ma, const CUtensorMap &mb, const CUtensorMap &mbh,
+                          const TcParams &tp, int clusters, cudaStream_t s) {
+    cudaLaunchAttribute attr[1];
+    cudaLaunchConfig_t lc = config(smem(), s, attr);
+    lc.gridDim = dim3((unsigned)(2 * clusters));
+    cudaError_t e = cudaLaunchKernelEx(&lc, tc2_gemm_kernel<BN, STAGES, ES>, ma, mb, mbh, tp);
+    if (e != cudaSuccess) return cuda_error(e, "tc2_gemm_kernel launch");
+    return MM_OK;
+  }
+};
+
+template <int ES>
+mm_status pair_capacity(int cfg, int *max_clusters) {
+  if (kCfgs[cfg].bn == 256) return PairKernel<256, 7, ES>::capacity(max_clusters);
+  return PairKernel<128, 8, ES>::capacity(max_clusters);
 }
 
 template <int ES>
 mm_status dispatch_pair(int cfg, const CUtensorMap &ma, const CUtensorMap &mb,
-                        const TcParams &tp, int64_t units, cudaStream_t s) {
-  if (kCfgs[cfg].bn == 256) return launch_pair_kernel<256, 6, ES>(ma, mb, tp, units, s);
-  return launch_pair_kernel<128, 8, ES>(ma, mb, tp, units, s);
+                        const CUtensorMap &mbh, const TcParams &tp, int clusters,
+                        cudaStream_t s) {
+  if (kCfgs[cfg].bn == 256) return PairKernel<256, 7, ES>::launch(ma, mb, mbh, tp, clusters, s);
+  return PairKernel<128, 8, ES>::launch(ma, mb, mbh, tp, clusters, s);
 }
 
 template <int ES>
@@ -1120,7 +1167,20 @@ mm_status launch_tc(const Problem &p, LaunchCtx &ctx, int cfg) {
     tp.splits = 1;
     tp.kb_per_split = tp.num_kb;
   }
-  const int64_t units = tiles * tp.splits;
+  int64_t units = tiles * tp.splits;
+  int pair_clusters = 0;
+  tp.full_units = (int)std::min<int64_t>(units, (1LL << 31) - 1);
+  if (c.pair) {
+    st = es == 2 ? pair_capacity<2>(cfg, &pair_clusters) : pair_capacity<4>(cfg, &pair_clusters);
+    if (st != MM_OK) return st;
+    // split the last partial wave's tiles in half along N when that keeps it
+    // within one round (only where a half tile still fills whole TMA boxes)
+    const int64_t rem = tiles % pair_clusters;
+    if (bn == 256 && tiles > pair_clusters && rem > 0 && 2 * rem <= pair_clusters) {
+      tp.full_units = (int)(tiles - rem);
+      units = tiles + rem;
+    }
+  }
   if (units >= (1LL << 31)) return set_error(MM_ERR_UNSUPPORTED, "too many work units");
   tp.total_units = (int)units;
   tp.C = p.C;
@@ -1135,12 +1195,13 @@ mm_status launch_tc(const Problem &p, LaunchCtx &ctx, int cfg) {
   tp.a_mn = p.at ? 1 : 0;
   tp.b_mn = p.bt ? 0 : 1;
   const uint32_t fmt = p.ta == MM_F16 ? 0u : p.ta == MM_BF16 ? 1u : 2u;
-  tp.idesc = (1u << 4)                        // D: f32
-             | (fmt << 7) | (fmt << 10)       // A, B types
-             | ((uint32_t)tp.a_mn << 15)      // A major (1 = MN)
-             | ((uint32_t)tp.b_mn << 16)      // B major (1 = MN)
-             | ((uint32_t)(bn >> 3) << 17)    // N / 8
-             | ((uint32_t)(tile_m >> 4) << 24);  // M / 16 (256 for a CTA pair)
+  const uint32_t idesc_base = (1u << 4)                  // D: f32
+                              | (fmt << 7) | (fmt << 10)  // A, B types
+                              | ((uint32_t)tp.a_mn << 15) // A major (1 = MN)
+                              | ((uint32_t)tp.b_mn << 16) // B major (1 = MN)
+                              | ((uint32_t)(tile_m >> 4) << 24);  // M / 16 (256 for a pair)
+  tp.idesc = idesc_base | ((uint32_t)(bn >> 3) << 17);             // N / 8
+  tp.idesc_half = idesc_base | ((uint32_t)(bn >> 4) << 17);        // N / 16: half width
   // K-major: 8-row groups 1024 B apart, K advances 32 B inside the swizzle row.
   // MN-major: boxes of 128 bytes x bk rows; atoms along MN are bk*128 B apart,
   // 8-row K groups 1024 B apart, K advances umma_k rows (umma_k * 128 B).
@@ -1153,9 +1214,17 @@ mm_status launch_tc(const Problem &p, LaunchCtx &ctx, int cfg) {
   tp.b_boxes = tp.b_mn ? bn_cta / atom : 1;
   tp.a_box_stride = mn_atom_bytes;
   tp.b_box_stride = mn_atom_bytes;
-  if (c.pair)
-    return es == 2 ? dispatch_pair<2>(cfg, ma, mb, tp, units, ctx.stream)
-                   : dispatch_pair<4>(cfg, ma, mb, tp, units, ctx.stream);
+  if (c.pair) {
+    // B map for half-width units (K-major B loads bn/4 rows per CTA)
+    CUtensorMap mbh = mb;
+    if (p.bt && tp.full_units < tp.total_units) {
+      st = encode_map(&mbh, p.tb, p.B, p.K, p.N, p.batch, p.ldb * es, p.sB * es, bk, bn_cta / 2);
+      if (st != MM_OK) return st;
+    }
+    const int clusters = (int)std::min<int64_t>(units, pair_clusters);
+    return es == 2 ? dispatch_pair<2>(cfg, ma, mb, mbh, tp, clusters, ctx.stream)
+                   : dispatch_pair<4>(cfg, ma, mb, mbh, tp, clusters, ctx.stream);
+  }
   if (tp.splits > 1) {
     void *w = nullptr;
     size_t ws_bytes = (size_t)tp.splits * tp.batch * (size_t)p.M * p.N * sizeof(float);
