@@ -6,8 +6,9 @@
 //
 //   * persistent: one CTA per SM walks the work units (output tile x batch x
 //     K split) with a grid stride;
-//   * warp-specialised, 6 warps: warp 0 issues TMA loads (one elected lane),
-//     warp 1 allocates TMEM and issues tcgen05.mma (one lane), warps 2..5
+//   * warp-specialised, 6 warps: warp 0 issues TMA loads, warp 1 allocates
+//     TMEM and issues tcgen05.mma (each role runs as a whole warp with
+//     warp-uniform loop state; elect.sync picks the issuing lane), warps 2..5
 //     drain accumulators from TMEM (tcgen05.ld) and store them;
 //   * an S-stage shared-memory ring guarded by mbarriers (full: TMA bytes
 //     landed; empty: the MMAs reading the stage completed, signalled by
@@ -76,9 +77,16 @@ __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
 }
 
+// The producer and MMA roles run as whole warps so that their loop state stays
+// warp-uniform; each issuing wrapper below marked "warp-collective" is executed
+// by all 32 lanes and elect.sync picks the one lane that performs the operation.
+
+// Warp-collective.
 __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-               : "memory");
+  asm volatile(
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n\t}" ::"r"(bar), "r"(bytes)
+      : "memory");
 }
 
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
@@ -103,24 +111,34 @@ __device__ __forceinline__ uint64_t global_ns() {
   return t;
 }
 
-// Wait for the phase of `parity` to complete.  Gives up (false) when the
-// shared abort flag is raised or after timeout_ns, raising the flag and
-// recording `code` in the error word.
-__device__ __noinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int *abort_flag,
-                                          int *err, int code, uint64_t timeout_ns) {
-  if (mbar_try_wait(bar, parity)) return true;
+// Wait for the phase of `parity` to complete.  Executed by a whole warp (every
+// lane polls; the result is warp-uniform).  Gives up (false) when the shared
+// abort flag is raised or after timeout_ns, raising the flag and recording
+// `code` in the error word.
+__device__ __noinline__ bool warp_wait_slow(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                            int *err, int code, uint64_t timeout_ns) {
   const uint64_t t0 = global_ns();
   while (true) {
 #pragma unroll 1
     for (int i = 0; i < 32; ++i)
-      if (mbar_try_wait(bar, parity)) return true;
-    if (*abort_flag) return false;
-    if (global_ns() - t0 > timeout_ns) {
-      *abort_flag = 1;
-      atomicCAS(err, 0, code);
-      return false;
+      if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
+    int stop = 0;
+    if ((threadIdx.x & 31) == 0) {
+      if (*abort_flag) {
+        stop = 1;
+      } else if (global_ns() - t0 > timeout_ns) {
+        *abort_flag = 1;
+        atomicCAS(err, 0, code);
+        stop = 1;
+      }
     }
+    if (__shfl_sync(0xffffffffu, stop, 0)) return false;
   }
+}
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                          int *err, int code, uint64_t timeout_ns) {
+  if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
+  return warp_wait_slow(bar, parity, abort_flag, err, code, timeout_ns);
 }
 
 // Bounded wait that ignores the abort flag: used at the end to let copies and
@@ -136,11 +154,13 @@ __device__ __noinline__ void wait_drain(uint32_t bar, uint32_t parity, int *err,
   }
 }
 
+// Warp-collective.
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, uint32_t bar,
                                             int c0, int c1, int c2) {
   asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5}], [%2];\n\t}" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
       : "memory");
 }
@@ -169,29 +189,33 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
                : "memory");
 }
 
+// Warp-collective.
 template <int ES>
 __device__ __forceinline__ void umma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
                                      uint32_t idesc, uint32_t accumulate) {
   if constexpr (ES == 2) {
     asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "{\n\t.reg .pred p, e;\n\tsetp.ne.b32 p, %4, 0;\n\telect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
         "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
         : "memory");
   } else {
     asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "{\n\t.reg .pred p, e;\n\tsetp.ne.b32 p, %4, 0;\n\telect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
         "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
         : "memory");
   }
 }
 
-// Arrive on `bar` once every previously issued tcgen05 op of this thread is done.
+// Arrive on `bar` once every previously issued tcgen05 op of the issuing
+// thread is done.  Warp-collective.
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                   bar)
-               : "memory");
+  asm volatile(
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(
+          bar)
+      : "memory");
 }
 
 // 32 lanes x 32 consecutive 32-bit columns: thread i gets row (lane) i.
@@ -347,8 +371,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const uint32_t tmem_base = *tmem_slot;
 
   if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
+    // ------------------------------------------------------------ TMA producer (whole warp)
+    {
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
@@ -358,8 +382,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int kb0 = sp * p.kb_per_split;
         const int kb1 = min(p.num_kb, kb0 + p.kb_per_split);
         for (int kb = kb0; kb < kb1; ++kb) {
-          if (!wait_bounded(empty0 + 8 * stage, phase ^ 1, abort_flag, p.err, kErrProducer,
-                            p.timeout_ns)) {
+          if (!warp_wait(empty0 + 8 * stage, phase ^ 1, abort_flag, p.err, kErrProducer,
+                         p.timeout_ns)) {
             ok = false;
             break;
           }
@@ -397,8 +421,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     __syncwarp();
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // ------------------------------------------------------------ MMA issuer (whole warp)
+    {
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
@@ -409,13 +433,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         decode_unit(p, u, tm, tn, b, sp);
         const int kb0 = sp * p.kb_per_split;
         const int kb1 = min(p.num_kb, kb0 + p.kb_per_split);
-        if (!wait_bounded(tempty0 + 8 * acc, acc_phase ^ 1, abort_flag, p.err, kErrMma,
-                          p.timeout_ns))
+        if (!warp_wait(tempty0 + 8 * acc, acc_phase ^ 1, abort_flag, p.err, kErrMma,
+                       p.timeout_ns))
           break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
         for (int kb = kb0; kb < kb1; ++kb) {
-          if (!wait_bounded(full0 + 8 * stage, phase, abort_flag, p.err, kErrMma, p.timeout_ns)) {
+          if (!warp_wait(full0 + 8 * stage, phase, abort_flag, p.err, kErrMma, p.timeout_ns)) {
             ok = false;
             break;
           }
@@ -454,12 +478,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     for (int u = blockIdx.x; u < p.total_units; u += gridDim.x) {
       int tm, tn, b, sp;
       decode_unit(p, u, tm, tn, b, sp);
-      int ok = 1;
-      if (lane == 0)
-        ok = wait_bounded(tfull0 + 8 * acc, acc_phase, abort_flag, p.err, kErrEpilogue,
-                          p.timeout_ns);
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) break;
+      if (!warp_wait(tfull0 + 8 * acc, acc_phase, abort_flag, p.err, kErrEpilogue, p.timeout_ns))
+        break;
       tc_fence_after();
       const int row = tm * BM + q * 32 + lane;
       const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
@@ -523,11 +543,13 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
                : "memory");
 }
+// Warp-collective.
 __device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap *map,
                                                  uint32_t leader_bar, int c0, int c1, int c2) {
   asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.cta_group::2"
-      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.cta_group::2"
+      " [%0], [%1, {%3, %4, %5}], [%2];\n\t}" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(leader_bar), "r"(c0), "r"(c1), "r"(c2)
       : "memory");
 }
@@ -543,37 +565,43 @@ __device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols
   asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
                : "memory");
 }
+// Warp-collective.
 template <int ES>
 __device__ __forceinline__ void umma_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
                                           uint32_t idesc, uint32_t accumulate) {
   if constexpr (ES == 2) {
     asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "{\n\t.reg .pred p, e;\n\tsetp.ne.b32 p, %4, 0;\n\telect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
         "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
         : "memory");
   } else {
     asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::2.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "{\n\t.reg .pred p, e;\n\tsetp.ne.b32 p, %4, 0;\n\telect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.mma.cta_group::2.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
         "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
         : "memory");
   }
 }
 // Arrive on the barrier at this offset in both CTAs of the pair once every
-// tcgen05 op issued so far by this thread has completed.
+// tcgen05 op issued so far by the issuing thread has completed.
+// Warp-collective.
 __device__ __forceinline__ void umma_commit_pair_both(uint32_t bar) {
   const uint16_t mask = 0x3;
   asm volatile(
-      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(bar),
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;\n\t}" ::"r"(bar),
       "h"(mask)
       : "memory");
 }
+// Warp-collective.
 __device__ __forceinline__ void umma_commit_pair_local(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                   bar)
-               : "memory");
+  asm volatile(
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(
+          bar)
+      : "memory");
 }
 
 constexpr uint32_t kPairSlack = 0;  // shared memory reserved after the ring
@@ -658,8 +686,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const uint32_t leader_tempty0 = map_to_rank(tempty0, 0);
 
   if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer (both CTAs)
-    if (lane == 0) {
+    // ------------------------------------------------------------ TMA producer (both CTAs, whole warp)
+    {
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
@@ -671,8 +699,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int n0 = t0 + (int)rank * nh;
         const uint32_t tx = 2 * (A_BYTES + (uint32_t)nh * 128);
         for (int kb = 0; kb < p.num_kb; ++kb) {
-          if (!wait_bounded(empty0 + 8 * stage, phase ^ 1, abort_flag, p.err, kErrProducer,
-                            p.timeout_ns)) {
+          if (!warp_wait(empty0 + 8 * stage, phase ^ 1, abort_flag, p.err, kErrProducer,
+                         p.timeout_ns)) {
             ok = false;
             break;
           }
@@ -708,8 +736,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     __syncwarp();
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer (leader)
-    if (lane == 0 && leader) {
+    // ------------------------------------------------------------ MMA issuer (leader, whole warp)
+    if (leader) {
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
@@ -719,13 +747,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         int tm_, t0_, b_, nw;
         pair_unit(p, u, BN, tm_, t0_, b_, nw);
         const uint32_t idesc = nw == BN ? p.idesc : p.idesc_half;
-        if (!wait_bounded(tempty0 + 8 * acc, acc_phase ^ 1, abort_flag, p.err, kErrMma,
-                          p.timeout_ns))
+        if (!warp_wait(tempty0 + 8 * acc, acc_phase ^ 1, abort_flag, p.err, kErrMma,
+                       p.timeout_ns))
           break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
         for (int kb = 0; kb < p.num_kb; ++kb) {
-          if (!wait_bounded(full0 + 8 * stage, phase, abort_flag, p.err, kErrMma, p.timeout_ns)) {
+          if (!warp_wait(full0 + 8 * stage, phase, abort_flag, p.err, kErrMma, p.timeout_ns)) {
             ok = false;
             break;
           }
@@ -763,12 +791,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     for (int u = cid; u < p.total_units; u += ncl) {
       int tm, n0, b, nw;
       pair_unit(p, u, BN, tm, n0, b, nw);
-      int ok = 1;
-      if (lane == 0)
-        ok = wait_bounded(tfull0 + 8 * acc, acc_phase, abort_flag, p.err, kErrEpilogue,
-                          p.timeout_ns);
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) break;
+      if (!warp_wait(tfull0 + 8 * acc, acc_phase, abort_flag, p.err, kErrEpilogue, p.timeout_ns))
+        break;
       tc_fence_after();
       const int row = tm * PAIR_M + (int)rank * BM + q * 32 + lane;
       const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
