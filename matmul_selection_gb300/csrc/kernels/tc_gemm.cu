@@ -61,6 +61,9 @@ struct TcParams {
   uint32_t a_kstep, b_kstep;         // start-address advance per MMA k-step (16-byte units)
   uint32_t a_box_stride, b_box_stride;  // bytes between the TMA boxes of one stage (MN-major)
   int a_boxes, b_boxes, a_mn, b_mn;
+  // MN-major operand whose boxes of one stage come from a single 4-D copy
+  // (map over (atom, K, atom index, batch)); 0: one 3-D copy per box
+  int a_4d, b_4d;
   uint64_t timeout_ns;
   // 2-SM kernel: units [0, full_units) are whole tiles; the remaining tiles
   // of the last partial wave are split along N into two half-width units
@@ -162,6 +165,17 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map
       "@e cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%3, %4, %5}], [%2];\n\t}" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+
+// Warp-collective.
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *map, uint32_t bar,
+                                            int c0, int c1, int c2, int c3) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6}], [%2];\n\t}" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
       : "memory");
 }
 
@@ -393,12 +407,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           mbar_expect_tx(fb, STAGE_BYTES);
           if (!p.a_mn) {
             tma_load_3d(sa, &tmA, fb, kb * BK, tm * BM, b);
+          } else if (p.a_4d) {
+            tma_load_4d(sa, &tmA, fb, 0, kb * BK, tm * (BM / ATOM), b);
           } else {
             for (int j = 0; j < p.a_boxes; ++j)
               tma_load_3d(sa + j * p.a_box_stride, &tmA, fb, tm * BM + j * ATOM, kb * BK, b);
           }
           if (!p.b_mn) {
             tma_load_3d(sb, &tmB, fb, kb * BK, tn * BN, b);
+          } else if (p.b_4d) {
+            tma_load_4d(sb, &tmB, fb, 0, kb * BK, tn * (BN / ATOM), b);
           } else {
             for (int j = 0; j < p.b_boxes; ++j)
               tma_load_3d(sb + j * p.b_box_stride, &tmB, fb, tn * BN + j * ATOM, kb * BK, b);
@@ -515,6 +533,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 // multicast to the "empty" and "tmem full" barriers of both CTAs; both CTAs'
 // epilogue warps arrive on the leader's "tmem empty" barrier.  Each SM thus
 // loads half as many B bytes per k-block as the single-SM form.
+//
+// CL = 2 puts two pairs side by side along N in one cluster of four (ranks
+// 0-1: pair 0, ranks 2-3: pair 1).  Both pairs need the same 256 rows of A:
+// each CTA loads half of its 128 rows and multicasts them to the CTA at the
+// same position in the other pair, so each A byte leaves L2 once for 512
+// output columns.  A stage of a CTA is then written by both pairs' producers,
+// so its "empty" barrier waits for both pairs' MMAs (one commit from each
+// leader, multicast to all four CTAs).
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
@@ -553,6 +579,30 @@ __device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap
       "l"(reinterpret_cast<uint64_t>(map)), "r"(leader_bar), "r"(c0), "r"(c1), "r"(c2)
       : "memory");
 }
+// The same copy delivered to every CTA in `mask` (same shared-memory offset in
+// each); each destination's bytes complete on the barrier at `leader_bar`'s
+// offset in the even CTA of that destination's pair.  Warp-collective.
+__device__ __forceinline__ void tma_load_3d_pair_mc(uint32_t dst, const CUtensorMap *map,
+                                                    uint32_t leader_bar, int c0, int c1, int c2,
+                                                    uint16_t mask) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      ".multicast::cluster.cta_group::2 [%0], [%1, {%3, %4, %5}], [%2], %6;\n\t}" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(leader_bar), "r"(c0), "r"(c1), "r"(c2), "h"(mask)
+      : "memory");
+}
+// Warp-collective.
+__device__ __forceinline__ void tma_load_4d_pair(uint32_t dst, const CUtensorMap *map,
+                                                 uint32_t leader_bar, int c0, int c1, int c2,
+                                                 int c3) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes.cta_group::2"
+      " [%0], [%1, {%3, %4, %5, %6}], [%2];\n\t}" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(leader_bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+      : "memory");
+}
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
                "r"(ncols)
@@ -583,11 +633,10 @@ __device__ __forceinline__ void umma_pair(uint32_t d_tmem, uint64_t adesc, uint6
         : "memory");
   }
 }
-// Arrive on the barrier at this offset in both CTAs of the pair once every
+// Arrive on the barrier at this offset in every CTA of `mask` once every
 // tcgen05 op issued so far by the issuing thread has completed.
 // Warp-collective.
-__device__ __forceinline__ void umma_commit_pair_both(uint32_t bar) {
-  const uint16_t mask = 0x3;
+__device__ __forceinline__ void umma_commit_multicast(uint32_t bar, uint16_t mask) {
   asm volatile(
       "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
       "@e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
@@ -623,7 +672,7 @@ __device__ __forceinline__ void pair_unit(const TcParams &p, int u, int bn, int 
   nw = half < 0 ? bn : bn / 2;
 }
 
-template <int BN, int STAGES, int ES>
+template <int BN, int STAGES, int ES, int CL>
 __global__ void __launch_bounds__(kTcThreads, 1)
     tc2_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                     const __grid_constant__ CUtensorMap tmB,
@@ -653,13 +702,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();
-  const bool leader = rank == 0;
+  const uint32_t pos = rank & 1u, pair = rank >> 1;  // position in the pair, pair in the cluster
+  const bool leader = pos == 0;
+  const uint16_t pair_mask = (uint16_t)(0x3u << (2 * pair));
+  const uint16_t all_mask = (uint16_t)((1u << (2 * CL)) - 1u);
   const int cid = (int)cluster_id_x(), ncl = (int)nclusters_x();
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full0 + 8 * s, 1);
-      mbar_init(empty0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, CL);  // one commit from each pair's leader
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull0 + 8 * a, 1);
@@ -682,8 +734,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   cluster_sync_all();  // barriers of both CTAs initialised before any remote use
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  const uint32_t leader_full0 = map_to_rank(full0, 0);
-  const uint32_t leader_tempty0 = map_to_rank(tempty0, 0);
+  const uint32_t leader_full0 = map_to_rank(full0, rank & ~1u);
+  const uint32_t leader_tempty0 = map_to_rank(tempty0, rank & ~1u);
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer (both CTAs, whole warp)
@@ -692,11 +744,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       uint32_t phase = 0;
       bool ok = true;
       for (int u = cid; u < p.total_units && ok; u += ncl) {
-        int tm, t0, b, nw;
-        pair_unit(p, u, BN, tm, t0, b, nw);
-        const int nh = nw / 2;  // B columns this CTA loads for the unit
-        const int m0 = tm * PAIR_M + (int)rank * BM;
-        const int n0 = t0 + (int)rank * nh;
+        int tm, t0, b, w;
+        pair_unit(p, u, CL * BN, tm, t0, b, w);
+        const int nw = w / CL;   // this pair's columns
+        const int nh = nw / 2;   // B columns this CTA loads for the unit
+        const int m0 = tm * PAIR_M + (int)pos * BM;
+        const int n0 = t0 + (int)pair * nw + (int)pos * nh;
         const uint32_t tx = 2 * (A_BYTES + (uint32_t)nh * 128);
         for (int kb = 0; kb < p.num_kb; ++kb) {
           if (!warp_wait(empty0 + 8 * stage, phase ^ 1, abort_flag, p.err, kErrProducer,
@@ -708,17 +761,33 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           const uint32_t sa = smem_u32(smem + stage * STAGE_BYTES);
           const uint32_t sb = sa + A_BYTES;
           if (leader) mbar_expect_tx(full0 + 8 * stage, tx);
-          if (!p.a_mn) {
-            tma_load_3d_pair(sa, &tmA, lfb, kb * BK, m0, b);
+          if constexpr (CL == 1) {
+            if (!p.a_mn) {
+              tma_load_3d_pair(sa, &tmA, lfb, kb * BK, m0, b);
+            } else if (p.a_4d) {
+              tma_load_4d_pair(sa, &tmA, lfb, 0, kb * BK, m0 / ATOM, b);
+            } else {
+              for (int j = 0; j < p.a_boxes; ++j)
+                tma_load_3d_pair(sa + j * p.a_box_stride, &tmA, lfb, m0 + j * ATOM, kb * BK, b);
+            }
           } else {
-            for (int j = 0; j < p.a_boxes; ++j)
-              tma_load_3d_pair(sa + j * p.a_box_stride, &tmA, lfb, m0 + j * ATOM, kb * BK, b);
+            // half of this CTA's A rows, to the same position in both pairs
+            const uint16_t amask = (uint16_t)(0x5u << pos);
+            if (!p.a_mn)  // box of BM / 2 rows
+              tma_load_3d_pair_mc(sa + pair * (BM / 2) * 128, &tmA, lfb, kb * BK,
+                                  m0 + (int)pair * (BM / 2), b, amask);
+            else          // one of the two 64-row boxes
+              tma_load_3d_pair_mc(sa + pair * p.a_box_stride, &tmA, lfb, m0 + (int)pair * ATOM,
+                                  kb * BK, b, amask);
           }
           if (!p.b_mn) {
             tma_load_3d_pair(sb, nw == BN ? &tmB : &tmBh, lfb, kb * BK, n0, b);
-          } else {
+          } else if (p.b_4d && nh == BNH) {
+            tma_load_4d_pair(sb, &tmB, lfb, 0, kb * BK, n0 / ATOM, b);
+          } else {  // with a 4-D map in tmB, tmBh holds the per-box 3-D map
             for (int j = 0; j < nh / ATOM; ++j)
-              tma_load_3d_pair(sb + j * p.b_box_stride, &tmB, lfb, n0 + j * ATOM, kb * BK, b);
+              tma_load_3d_pair(sb + j * p.b_box_stride, p.b_4d ? &tmBh : &tmB, lfb, n0 + j * ATOM,
+                               kb * BK, b);
           }
           if (++stage == STAGES) {
             stage = 0;
@@ -744,9 +813,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       uint32_t acc_phase = 0;
       bool ok = true;
       for (int u = cid; u < p.total_units && ok; u += ncl) {
-        int tm_, t0_, b_, nw;
-        pair_unit(p, u, BN, tm_, t0_, b_, nw);
-        const uint32_t idesc = nw == BN ? p.idesc : p.idesc_half;
+        int tm_, t0_, b_, w;
+        pair_unit(p, u, CL * BN, tm_, t0_, b_, w);
+        const uint32_t idesc = w == CL * BN ? p.idesc : p.idesc_half;
         if (!warp_wait(tempty0 + 8 * acc, acc_phase ^ 1, abort_flag, p.err, kErrMma,
                        p.timeout_ns))
           break;
@@ -766,14 +835,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           for (int kk = 0; kk < KSTEPS; ++kk)
             umma_pair<ES>(d_tmem, adesc + (uint64_t)(kk * p.a_kstep),
                           bdesc + (uint64_t)(kk * p.b_kstep), idesc, (kb > 0 || kk > 0) ? 1u : 0u);
-          umma_commit_pair_both(empty0 + 8 * stage);
+          umma_commit_multicast(empty0 + 8 * stage, all_mask);
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1;
           }
         }
         if (!ok) break;
-        umma_commit_pair_both(tfull0 + 8 * acc);
+        umma_commit_multicast(tfull0 + 8 * acc, pair_mask);
         if (++acc == 2) {
           acc = 0;
           acc_phase ^= 1;
@@ -789,12 +858,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int u = cid; u < p.total_units; u += ncl) {
-      int tm, n0, b, nw;
-      pair_unit(p, u, BN, tm, n0, b, nw);
+      int tm, t0, b, w;
+      pair_unit(p, u, CL * BN, tm, t0, b, w);
+      const int nw = w / CL, n0 = t0 + (int)pair * nw;
       if (!warp_wait(tfull0 + 8 * acc, acc_phase, abort_flag, p.err, kErrEpilogue, p.timeout_ns))
         break;
       tc_fence_after();
-      const int row = tm * PAIR_M + (int)rank * BM + q * 32 + lane;
+      const int row = tm * PAIR_M + (int)pos * BM + q * 32 + lane;
       const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
 #pragma unroll 1
       for (int c = 0; c < nw / 32; ++c) {
@@ -814,7 +884,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
-  cluster_sync_all();  // the leader's MMAs (reading both CTAs' smem, writing both TMEMs) are done
+  // the leaders' MMAs (reading both CTAs' smem, writing both TMEMs) are done;
+  // with CL = 2 the other pair's copies into this CTA completed on our
+  // leader's barriers, which its producer drained
+  cluster_sync_all();
   tc_fence_after();
   if (warp == 1) tmem_dealloc_pair(tmem_base, TMEM_COLS);
 }
@@ -847,16 +920,18 @@ struct TcCfg {
   int stages;
   bool splitk;
   bool pair;    // 2-SM (cta_group::2) kernel, tile M = 256
+  int cl;       // pairs per cluster (2: two pairs along N share A by multicast)
 };
 
 const TcCfg kCfgs[] = {
-    {"tc_128x256_s4", 256, 4, false, false},
-    {"tc_128x128_s6", 128, 6, false, false},
-    {"tc_128x64_s8", 64, 8, false, false},
-    {"tc_splitk_128x128_s6", 128, 6, true, false},
-    {"tc_splitk_128x64_s8", 64, 8, true, false},
-    {"tc2_256x256_s7", 256, 7, false, true},
-    {"tc2_256x128_s8", 128, 8, false, true},
+    {"tc_128x256_s4", 256, 4, false, false, 1},
+    {"tc_128x128_s6", 128, 6, false, false, 1},
+    {"tc_128x64_s8", 64, 8, false, false, 1},
+    {"tc_splitk_128x128_s6", 128, 6, true, false, 1},
+    {"tc_splitk_128x64_s8", 64, 8, true, false, 1},
+    {"tc2_256x256_s7", 256, 7, false, true, 1},
+    {"tc2_256x128_s8", 128, 8, false, true, 1},
+    {"tc2x2_256x256_s7", 256, 7, false, true, 2},
 };
 
 size_t smem_bytes(int bn, int stages) {
@@ -907,6 +982,30 @@ mm_status encode_map(CUtensorMap *map, int dtype, const void *base, uint64_t inn
   return MM_OK;
 }
 
+// 4-D map over an MN-major operand stored as `outer` rows (K) of `inner`
+// contiguous elements (M or N): dims (atom, K, inner / atom, batch), so one
+// copy brings `nboxes` consecutive atom-wide boxes, laid out in shared memory
+// exactly as nboxes separate 3-D boxes.  Needs inner % atom == 0 (an atom never
+// crosses the end of a row, so out-of-range atoms still read the fill value).
+mm_status encode_map4(CUtensorMap *map, int dtype, const void *base, uint64_t inner,
+                      uint64_t outer, uint64_t batch, uint64_t ld_bytes, uint64_t bstride_bytes,
+                      uint32_t atom, uint32_t box_k, uint32_t nboxes) {
+  auto fn = encode_fn();
+  if (!fn) return set_error(MM_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
+  const int es = dtype == MM_F32 ? 4 : 2;
+  cuuint64_t dims[4] = {atom, outer, inner / atom, batch};
+  if (batch <= 1) bstride_bytes = ((ld_bytes * outer) + 15) & ~(uint64_t)15;
+  cuuint64_t strides[3] = {ld_bytes, (uint64_t)atom * es, bstride_bytes};
+  cuuint32_t box[4] = {atom, box_k, nboxes, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = fn(map, map_dtype(dtype), 4, const_cast<void *>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return set_error(MM_ERR_CUDA, "cuTensorMapEncodeTiled (4-D) failed (%d)", (int)r);
+  return MM_OK;
+}
+
 uint64_t smem_desc_bits(uint32_t lbo_bytes, uint32_t sbo_bytes) {
   uint64_t d = 0;
   d |= (uint64_t)((lbo_bytes >> 4) & 0x3FFFu) << 16;  // leading-dimension byte offset
@@ -933,12 +1032,12 @@ mm_status launch_kernel(const CUtensorMap &ma, const CUtensorMap &mb, const TcPa
   return MM_OK;
 }
 
-template <int BN, int STAGES, int ES>
+template <int BN, int STAGES, int ES, int CL>
 struct PairKernel {
   static cudaLaunchConfig_t config(size_t smem, cudaStream_t s, cudaLaunchAttribute *attr) {
     cudaLaunchConfig_t lc = {};
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.x = 2 * CL;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     lc.blockDim = dim3(kTcThreads);
@@ -949,7 +1048,7 @@ struct PairKernel {
     return lc;
   }
   static size_t smem() {
-    const TcCfg shape{"", BN, STAGES, false, true};
+    const TcCfg shape{"", BN, STAGES, false, true, CL};
     return smem_bytes_cfg(shape);
   }
   // Set-up once: shared-memory attribute and how many pairs fit at once.
@@ -958,17 +1057,17 @@ struct PairKernel {
     static cudaError_t err = cudaSuccess;
     static int clusters = 0;
     std::call_once(once, [] {
-      auto kern = tc2_gemm_kernel<BN, STAGES, ES>;
+      auto kern = tc2_gemm_kernel<BN, STAGES, ES, CL>;
       err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem());
       if (err == cudaSuccess) {
         cudaLaunchAttribute attr[1];
         cudaLaunchConfig_t q = config(smem(), nullptr, attr);
-        q.gridDim = dim3(2);
+        q.gridDim = dim3(2 * CL);
         err = cudaOccupancyMaxActiveClusters(&clusters, kern, &q);
       }
     });
     if (err != cudaSuccess) return cuda_error(err, "tc2 kernel set-up");
-    if (clusters < 1) return set_error(MM_ERR_UNSUPPORTED, "no CTA pair fits on this device");
+    if (clusters < 1) return set_error(MM_ERR_UNSUPPORTED, "no cluster of CTA pairs fits on this device");
     *max_clusters = clusters;
     return MM_OK;
   }
@@ -976,8 +1075,8 @@ struct PairKernel {
                           const TcParams &tp, int clusters, cudaStream_t s) {
     cudaLaunchAttribute attr[1];
     cudaLaunchConfig_t lc = config(smem(), s, attr);
-    lc.gridDim = dim3((unsigned)(2 * clusters));
-    cudaError_t e = cudaLaunchKernelEx(&lc, tc2_gemm_kernel<BN, STAGES, ES>, ma, mb, mbh, tp);
+    lc.gridDim = dim3((unsigned)(2 * CL * clusters));
+    cudaError_t e = cudaLaunchKernelEx(&lc, tc2_gemm_kernel<BN, STAGES, ES, CL>, ma, mb, mbh, tp);
     if (e != cudaSuccess) return cuda_error(e, "tc2_gemm_kernel launch");
     return MM_OK;
   }
@@ -985,16 +1084,18 @@ struct PairKernel {
 
 template <int ES>
 mm_status pair_capacity(int cfg, int *max_clusters) {
-  if (kCfgs[cfg].bn == 256) return PairKernel<256, 7, ES>::capacity(max_clusters);
-  return PairKernel<128, 8, ES>::capacity(max_clusters);
+  if (kCfgs[cfg].cl == 2) return PairKernel<256, 7, ES, 2>::capacity(max_clusters);
+  if (kCfgs[cfg].bn == 256) return PairKernel<256, 7, ES, 1>::capacity(max_clusters);
+  return PairKernel<128, 8, ES, 1>::capacity(max_clusters);
 }
 
 template <int ES>
 mm_status dispatch_pair(int cfg, const CUtensorMap &ma, const CUtensorMap &mb,
                         const CUtensorMap &mbh, const TcParams &tp, int clusters,
                         cudaStream_t s) {
-  if (kCfgs[cfg].bn == 256) return PairKernel<256, 7, ES>::launch(ma, mb, mbh, tp, clusters, s);
-  return PairKernel<128, 8, ES>::launch(ma, mb, mbh, tp, clusters, s);
+  if (kCfgs[cfg].cl == 2) return PairKernel<256, 7, ES, 2>::launch(ma, mb, mbh, tp, clusters, s);
+  if (kCfgs[cfg].bn == 256) return PairKernel<256, 7, ES, 1>::launch(ma, mb, mbh, tp, clusters, s);
+  return PairKernel<128, 8, ES, 1>::launch(ma, mb, mbh, tp, clusters, s);
 }
 
 template <int ES>
@@ -1160,11 +1261,14 @@ mm_status launch_tc(const Problem &p, LaunchCtx &ctx, int cfg) {
   const int bn = c.bn;
   const int bn_cta = c.pair ? bn / 2 : bn;  // B columns one CTA loads
   const int tile_m = c.pair ? 2 * BM : BM;
+  const int group_n = c.pair ? bn * c.cl : bn;  // columns of one work unit
   CUtensorMap ma, mb;
   mm_status st;
   // A: logical M x K.  K-major when stored row-major (N), MN-major when T.
+  // With two pairs per cluster each CTA loads half of its rows.
   if (!p.at)
-    st = encode_map(&ma, p.ta, p.A, p.K, p.M, p.batch, p.lda * es, p.sA * es, bk, BM);
+    st = encode_map(&ma, p.ta, p.A, p.K, p.M, p.batch, p.lda * es, p.sA * es, bk,
+                    c.cl == 2 ? BM / 2 : BM);
   else
     st = encode_map(&ma, p.ta, p.A, p.M, p.K, p.batch, p.lda * es, p.sA * es, atom, bk);
   if (st != MM_OK) return st;
@@ -1174,15 +1278,31 @@ mm_status launch_tc(const Problem &p, LaunchCtx &ctx, int cfg) {
   else
     st = encode_map(&mb, p.tb, p.B, p.N, p.K, p.batch, p.ldb * es, p.sB * es, atom, bk);
   if (st != MM_OK) return st;
+  // MN-major operands: one 4-D copy per stage instead of one copy per
+  // 128-byte-wide box, where the MN extent is a whole number of boxes
+  const int a_nbox = BM / atom, b_nbox = bn_cta / atom;
+  const bool a_4d = p.at && c.cl == 1 && a_nbox > 1 && p.M % atom == 0;
+  const bool b_4d = !p.bt && b_nbox > 1 && p.N % atom == 0;
+  const CUtensorMap mb3 = mb;  // per-box map (half-width units of the pair kernel)
+  if (a_4d) {
+    st = encode_map4(&ma, p.ta, p.A, p.M, p.K, p.batch, p.lda * es, p.sA * es, atom, bk, a_nbox);
+    if (st != MM_OK) return st;
+  }
+  if (b_4d) {
+    st = encode_map4(&mb, p.tb, p.B, p.N, p.K, p.batch, p.ldb * es, p.sB * es, atom, bk, b_nbox);
+    if (st != MM_OK) return st;
+  }
 
   TcParams tp;
   std::memset(&tp, 0, sizeof tp);
+  tp.a_4d = a_4d ? 1 : 0;
+  tp.b_4d = b_4d ? 1 : 0;
   tp.M = (int)p.M;
   tp.N = (int)p.N;
   tp.K = (int)p.K;
   tp.batch = (int)p.batch;
   tp.tiles_m = (int)ceil_div(p.M, tile_m);
-  tp.tiles_n = (int)ceil_div(p.N, bn);
+  tp.tiles_n = (int)ceil_div(p.N, group_n);
   tp.num_kb = (int)ceil_div(p.K, bk);
   const int64_t tiles = (int64_t)tp.tiles_m * tp.tiles_n * tp.batch;
   if (c.splitk) {
@@ -1240,7 +1360,7 @@ mm_status launch_tc(const Problem &p, LaunchCtx &ctx, int cfg) {
   tp.b_box_stride = mn_atom_bytes;
   if (c.pair) {
     // B map for half-width units (K-major B loads bn/4 rows per CTA)
-    CUtensorMap mbh = mb;
+    CUtensorMap mbh = b_4d ? mb3 : mb;
     if (p.bt && tp.full_units < tp.total_units) {
       st = encode_map(&mbh, p.tb, p.B, p.K, p.N, p.batch, p.ldb * es, p.sB * es, bk, bn_cta / 2);
       if (st != MM_OK) return st;
