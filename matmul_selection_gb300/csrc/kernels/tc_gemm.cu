@@ -6,10 +6,11 @@
 //
 //   * persistent: one CTA per SM walks the work units (output tile x batch x
 //     K split) with a grid stride;
-//   * warp-specialised, 6 warps: warp 0 issues TMA loads, warp 1 allocates
-//     TMEM and issues tcgen05.mma (each role runs as a whole warp with
-//     warp-uniform loop state; elect.sync picks the issuing lane), warps 2..5
-//     drain accumulators from TMEM (tcgen05.ld) and store them;
+//   * warp-specialised, 7 warps: warps 0 and 6 issue the TMA loads of A and
+//     of B, warp 1 allocates TMEM and issues tcgen05.mma (each role runs as a
+//     whole warp with warp-uniform loop state; elect.sync picks the issuing
+//     lane), warps 2..5 drain accumulators from TMEM (tcgen05.ld) and store
+//     them;
 //   * an S-stage shared-memory ring guarded by mbarriers (full: TMA bytes
 //     landed; empty: the MMAs reading the stage completed, signalled by
 //     tcgen05.commit), and two TMEM accumulators so the epilogue of one tile
@@ -41,7 +42,8 @@ namespace mm {
 namespace {
 
 constexpr int BM = 128;
-constexpr int kTcThreads = 192;
+// 7 warps: A copies, MMA, 4 epilogue warps, B copies
+constexpr int kTcThreads = 224;
 constexpr uint64_t kWaitTimeoutNs = 2000000000ull;  // 2 s per wait
 
 // error codes (first one wins): 0x100 | role
@@ -384,8 +386,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer (whole warp)
+  if (warp == 0 || warp == 6) {
+    // ------------------------------------------------------------ TMA producers
+    // warp 0 arms the stage and copies A, warp 6 copies B (see the 2-SM
+    // kernel for why B bytes landing before the arming are harmless)
+    const bool copy_a = warp == 0;
     {
       int stage = 0;
       uint32_t phase = 0;
@@ -404,16 +409,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           const uint32_t fb = full0 + 8 * stage;
           const uint32_t sa = smem_u32(smem + stage * STAGE_BYTES);
           const uint32_t sb = sa + A_BYTES;
-          mbar_expect_tx(fb, STAGE_BYTES);
-          if (!p.a_mn) {
-            tma_load_3d(sa, &tmA, fb, kb * BK, tm * BM, b);
-          } else if (p.a_4d) {
-            tma_load_4d(sa, &tmA, fb, 0, kb * BK, tm * (BM / ATOM), b);
-          } else {
-            for (int j = 0; j < p.a_boxes; ++j)
-              tma_load_3d(sa + j * p.a_box_stride, &tmA, fb, tm * BM + j * ATOM, kb * BK, b);
-          }
-          if (!p.b_mn) {
+          if (copy_a) {
+            mbar_expect_tx(fb, STAGE_BYTES);
+            if (!p.a_mn) {
+              tma_load_3d(sa, &tmA, fb, kb * BK, tm * BM, b);
+            } else if (p.a_4d) {
+              tma_load_4d(sa, &tmA, fb, 0, kb * BK, tm * (BM / ATOM), b);
+            } else {
+              for (int j = 0; j < p.a_boxes; ++j)
+                tma_load_3d(sa + j * p.a_box_stride, &tmA, fb, tm * BM + j * ATOM, kb * BK, b);
+            }
+          } else if (!p.b_mn) {
             tma_load_3d(sb, &tmB, fb, kb * BK, tn * BN, b);
           } else if (p.b_4d) {
             tma_load_4d(sb, &tmB, fb, 0, kb * BK, tn * (BN / ATOM), b);
@@ -430,11 +436,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       // Leave no copy in flight: wait until the MMA warp has released every
       // stage we filled (normal path), or at least until our last fills
       // landed (abort path).
-      for (int s = 0; s < STAGES; ++s) {
-        // the most recent fill of `stage` (walking backwards) used parity:
-        int st = (stage + s) % STAGES;
-        uint32_t par = (st < stage) ? phase : phase ^ 1;  // last completed-or-pending fill
-        wait_drain(full0 + 8 * st, par, p.err, kErrProducer, p.timeout_ns);
+      if (copy_a) {
+        for (int s = 0; s < STAGES; ++s) {
+          // the most recent fill of `stage` (walking backwards) used parity:
+          int st = (stage + s) % STAGES;
+          uint32_t par = (st < stage) ? phase : phase ^ 1;  // last completed-or-pending fill
+          wait_drain(full0 + 8 * st, par, p.err, kErrProducer, p.timeout_ns);
+        }
       }
     }
     __syncwarp();
@@ -516,6 +524,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         acc_phase ^= 1;
       }
     }
+  }
+  // after an abort, B copies may have been issued into stages never armed:
+  // give them time to land before shared memory is released
+  if (*abort_flag) {
+    const uint64_t t0 = global_ns();
+    while (global_ns() - t0 < 100000ull) __nanosleep(1000);
   }
   tc_fence_before();
   __syncthreads();
@@ -737,8 +751,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const uint32_t leader_full0 = map_to_rank(full0, rank & ~1u);
   const uint32_t leader_tempty0 = map_to_rank(tempty0, rank & ~1u);
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer (both CTAs, whole warp)
+  if (warp == 0 || warp == 6) {
+    // ------------------------------------------------------------ TMA producers (both CTAs)
+    // warp 0 arms the stage and copies A, warp 6 copies B; both wait on the
+    // same "empty" barrier.  B bytes may land before the arming: the barrier's
+    // transaction count goes transiently negative and its single arrival (the
+    // arming) still holds the phase open until A has landed too.
+    const bool copy_a = warp == 0;
     {
       int stage = 0;
       uint32_t phase = 0;
@@ -760,27 +779,28 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           const uint32_t lfb = leader_full0 + 8 * stage;
           const uint32_t sa = smem_u32(smem + stage * STAGE_BYTES);
           const uint32_t sb = sa + A_BYTES;
-          if (leader) mbar_expect_tx(full0 + 8 * stage, tx);
-          if constexpr (CL == 1) {
-            if (!p.a_mn) {
-              tma_load_3d_pair(sa, &tmA, lfb, kb * BK, m0, b);
-            } else if (p.a_4d) {
-              tma_load_4d_pair(sa, &tmA, lfb, 0, kb * BK, m0 / ATOM, b);
+          if (copy_a) {
+            if (leader) mbar_expect_tx(full0 + 8 * stage, tx);
+            if constexpr (CL == 1) {
+              if (!p.a_mn) {
+                tma_load_3d_pair(sa, &tmA, lfb, kb * BK, m0, b);
+              } else if (p.a_4d) {
+                tma_load_4d_pair(sa, &tmA, lfb, 0, kb * BK, m0 / ATOM, b);
+              } else {
+                for (int j = 0; j < p.a_boxes; ++j)
+                  tma_load_3d_pair(sa + j * p.a_box_stride, &tmA, lfb, m0 + j * ATOM, kb * BK, b);
+              }
             } else {
-              for (int j = 0; j < p.a_boxes; ++j)
-                tma_load_3d_pair(sa + j * p.a_box_stride, &tmA, lfb, m0 + j * ATOM, kb * BK, b);
+              // half of this CTA's A rows, to the same position in both pairs
+              const uint16_t amask = (uint16_t)(0x5u << pos);
+              if (!p.a_mn)  // box of BM / 2 rows
+                tma_load_3d_pair_mc(sa + pair * (BM / 2) * 128, &tmA, lfb, kb * BK,
+                                    m0 + (int)pair * (BM / 2), b, amask);
+              else          // one of the two 64-row boxes
+                tma_load_3d_pair_mc(sa + pair * p.a_box_stride, &tmA, lfb, m0 + (int)pair * ATOM,
+                                    kb * BK, b, amask);
             }
-          } else {
-            // half of this CTA's A rows, to the same position in both pairs
-            const uint16_t amask = (uint16_t)(0x5u << pos);
-            if (!p.a_mn)  // box of BM / 2 rows
-              tma_load_3d_pair_mc(sa + pair * (BM / 2) * 128, &tmA, lfb, kb * BK,
-                                  m0 + (int)pair * (BM / 2), b, amask);
-            else          // one of the two 64-row boxes
-              tma_load_3d_pair_mc(sa + pair * p.a_box_stride, &tmA, lfb, m0 + (int)pair * ATOM,
-                                  kb * BK, b, amask);
-          }
-          if (!p.b_mn) {
+          } else if (!p.b_mn) {
             tma_load_3d_pair(sb, nw == BN ? &tmB : &tmBh, lfb, kb * BK, n0, b);
           } else if (p.b_4d && nh == BNH) {
             tma_load_4d_pair(sb, &tmB, lfb, 0, kb * BK, n0 / ATOM, b);
@@ -796,7 +816,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
       }
       // the leader's full barriers see both CTAs' copies land
-      if (leader)
+      if (leader && copy_a)
         for (int s = 0; s < STAGES; ++s) {
           int st = (stage + s) % STAGES;
           uint32_t par = (st < stage) ? phase : phase ^ 1;
@@ -884,6 +904,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
+  // After an abort, copies issued into stages that were never armed (B copies
+  // ahead of the arming, the other pair's multicasts) are not covered by the
+  // drain above: give any such copy time to land before shared memory is
+  // released.
+  if (*abort_flag) {
+    const uint64_t t0 = global_ns();
+    while (global_ns() - t0 < 100000ull) __nanosleep(1000);
+  }
   // the leaders' MMAs (reading both CTAs' smem, writing both TMEMs) are done;
   // with CL = 2 the other pair's copies into this CTA completed on our
   // leader's barriers, which its producer drained
