@@ -18,6 +18,54 @@
 
 #include "../../include/mm.h"
 
+#include <utility>
+
+namespace mm {
+
+// Programmatic dependent launch.  Every kernel of the library is launched
+// with the programmatic-serialization attribute and begins with
+// pdl_launch_dependents() (the next kernel on the stream may be scheduled
+// into SM slots this grid leaves free) and pdl_wait() (block until the
+// previous kernel on the stream has completed and its writes are visible)
+// before it touches global memory.  Stream order is thus unchanged for memory;
+// what overlaps is the launch of a kernel with the tail of its predecessor.
+// Launched without the attribute, pdl_wait() returns at once.
+#ifdef __CUDACC__
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+#endif
+
+// Launch `kern` with the programmatic-serialization attribute and, unless
+// `cluster` is 1 x 1 x 1, that cluster shape.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       dim3 cluster, Args &&...args) {
+  cudaLaunchAttribute at[2];
+  unsigned n = 0;
+  at[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[n].val.programmaticStreamSerializationAllowed = 1;
+  ++n;
+  if (cluster.x * cluster.y * cluster.z > 1) {
+    at[n].id = cudaLaunchAttributeClusterDimension;
+    at[n].val.clusterDim.x = cluster.x;
+    at[n].val.clusterDim.y = cluster.y;
+    at[n].val.clusterDim.z = cluster.z;
+    ++n;
+  }
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = grid;
+  lc.blockDim = block;
+  lc.dynamicSmemBytes = smem;
+  lc.stream = s;
+  lc.attrs = at;
+  lc.numAttrs = n;
+  return cudaLaunchKernelEx(&lc, kern, std::forward<Args>(args)...);
+}
+
+}  // namespace mm
+
 namespace mm {
 
 constexpr const char *kVersion = "0.1.0";
@@ -254,6 +302,11 @@ const char *repack_config_name(int cfg);
 
 bool tc_supports(const Problem &p, const DeviceInfo &d, int cfg, std::string *why);
 mm_status launch_tc(const Problem &p, LaunchCtx &ctx, int cfg);
+// The same configurations on C^T = B^T A^T (operands exchanged, M and N
+// swapped, C written transposed): small M becomes the tile's N side.
+Problem swap_problem(const Problem &p);
+bool tc_swap_supports(const Problem &p, const DeviceInfo &d, int cfg, std::string *why);
+mm_status launch_tc_swapped(const Problem &p, LaunchCtx &ctx, int cfg);
 int tc_config_count();
 const char *tc_config_name(int cfg);
 bool tc_config_is_splitk(int cfg);

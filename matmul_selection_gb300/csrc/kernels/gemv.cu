@@ -161,6 +161,8 @@ __device__ void finish_tile(const GemvArgs &g, int b, int tile, int s, int col0,
 // ---------------------------------------------------------------- gemv_n
 template <int MT, int TB>
 __global__ void __launch_bounds__(kThreads) gemv_n_kernel(GemvArgs g) {
+  pdl_launch_dependents();
+  pdl_wait();
   constexpr int EB = TB == MM_F32 ? 4 : 2;
   constexpr int VEC = 16 / EB;
   constexpr int TN = 32 * VEC;
@@ -226,6 +228,8 @@ __global__ void __launch_bounds__(kThreads) gemv_n_kernel(GemvArgs g) {
 // ---------------------------------------------------------------- gemv_t
 template <int MT, int TB, int R>
 __global__ void __launch_bounds__(kThreads) gemv_t_kernel(GemvArgs g) {
+  pdl_launch_dependents();
+  pdl_wait();
   constexpr int EB = TB == MM_F32 ? 4 : 2;
   constexpr int VEC = 16 / EB;
   constexpr int NB = kWarps * R;  // output columns per block
@@ -307,9 +311,9 @@ int mt_for(int64_t M) { return M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : M <= 8 ? 8
 template <int MT, int TB>
 void launch_mt(const GemvArgs &g, bool bt, dim3 grid, size_t smem, cudaStream_t s) {
   if (bt)
-    gemv_t_kernel<MT, TB, kGemvR><<<grid, kThreads, smem, s>>>(g);
+    launch_pdl(gemv_t_kernel<MT, TB, kGemvR>, grid, dim3(kThreads), smem, s, dim3(1), g);
   else
-    gemv_n_kernel<MT, TB><<<grid, kThreads, smem, s>>>(g);
+    launch_pdl(gemv_n_kernel<MT, TB>, grid, dim3(kThreads), smem, s, dim3(1), g);
 }
 
 template <int TB>

@@ -129,6 +129,8 @@ __device__ __forceinline__ void stage_batched(const FastArgs &g, float *dst, int
 // ---------------------------------------------------------------- gemv_n_cluster
 template <int MT, int TB>
 __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1) gemv_n_cluster_kernel(const FastArgs g) {
+  pdl_launch_dependents();
+  pdl_wait();
   constexpr int EB = TB == MM_F32 ? 4 : 2;
   constexpr int VEC = 16 / EB;
   constexpr int CW = 256 / EB;          // columns per group: 256 bytes of a row
@@ -258,6 +260,8 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1) gemv_n_cluster_kern
 // ---------------------------------------------------------------- gemv_t_rows
 template <int MT, int TB>
 __global__ void __launch_bounds__(kThreads, MT <= 2 ? 2 : 1) gemv_t_rows_kernel(const FastArgs g) {
+  pdl_launch_dependents();
+  pdl_wait();
   constexpr int EB = TB == MM_F32 ? 4 : 2;
   constexpr int VEC = 16 / EB;
   constexpr int U = 8;
@@ -356,19 +360,8 @@ mm_status launch_n(const FastArgs &g, int groups, size_t smem, cudaStream_t s) {
   auto kern = gemv_n_cluster_kernel<MT, TB>;
   cudaError_t e = smem_attr(kern, smem);
   if (e != cudaSuccess) return cuda_error(e, "gemv_n_cluster smem attribute");
-  cudaLaunchConfig_t lc = {};
-  cudaLaunchAttribute at[1];
-  at[0].id = cudaLaunchAttributeClusterDimension;
-  at[0].val.clusterDim.x = 1;
-  at[0].val.clusterDim.y = kCluster;
-  at[0].val.clusterDim.z = 1;
-  lc.gridDim = dim3((unsigned)groups, kCluster, (unsigned)g.batch);
-  lc.blockDim = dim3(kThreads);
-  lc.dynamicSmemBytes = smem;
-  lc.stream = s;
-  lc.attrs = at;
-  lc.numAttrs = 1;
-  e = cudaLaunchKernelEx(&lc, kern, g);
+  e = launch_pdl(kern, dim3((unsigned)groups, kCluster, (unsigned)g.batch), dim3(kThreads), smem,
+                 s, dim3(1, kCluster, 1), g);
   return e == cudaSuccess ? MM_OK : cuda_error(e, "gemv_n_cluster launch");
 }
 
@@ -378,8 +371,7 @@ mm_status launch_t(const FastArgs &g, size_t smem, cudaStream_t s) {
   cudaError_t e = smem_attr(kern, smem);
   if (e != cudaSuccess) return cuda_error(e, "gemv_t_rows smem attribute");
   dim3 grid((unsigned)((g.N + kWarps - 1) / kWarps), (unsigned)g.batch);
-  kern<<<grid, kThreads, smem, s>>>(g);
-  e = cudaGetLastError();
+  e = launch_pdl(kern, grid, dim3(kThreads), smem, s, dim3(1), g);
   return e == cudaSuccess ? MM_OK : cuda_error(e, "gemv_t_rows launch");
 }
 

@@ -36,6 +36,8 @@ __global__ void naive_kernel(const void *__restrict__ A, const void *__restrict_
                              int64_t a_rs, int64_t a_cs, int64_t a_bs, int64_t b_rs,
                              int64_t b_cs, int64_t b_bs, int64_t ldc, int64_t c_bs,
                              int64_t batch) {
+  pdl_launch_dependents();
+  pdl_wait();
   int64_t j = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (j >= N) return;
   for (int64_t b = blockIdx.z; b < batch; b += gridDim.z) {
@@ -55,8 +57,8 @@ template <int TA, int TB>
 void launch_t(const Problem &p, cudaStream_t s, dim3 grid, dim3 block) {
   int64_t a_rs = p.at ? 1 : p.lda, a_cs = p.at ? p.lda : 1;
   int64_t b_rs = p.bt ? 1 : p.ldb, b_cs = p.bt ? p.ldb : 1;
-  naive_kernel<TA, TB><<<grid, block, 0, s>>>(p.A, p.B, p.C, p.tc, p.M, p.N, p.K, a_rs, a_cs,
-                                               p.sA, b_rs, b_cs, p.sB, p.ldc, p.sC, p.batch);
+  launch_pdl(naive_kernel<TA, TB>, grid, block, 0, s, dim3(1), p.A, p.B, p.C, p.tc, p.M, p.N, p.K,
+             a_rs, a_cs, p.sA, b_rs, b_cs, p.sB, p.ldc, p.sC, p.batch);
 }
 
 }  // namespace

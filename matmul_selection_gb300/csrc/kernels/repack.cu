@@ -23,6 +23,8 @@ template <int G>
 __global__ void repack_kernel(const char *__restrict__ src, char *__restrict__ dst, int64_t rows,
                               int64_t row_bytes, int64_t src_ld, int64_t dst_ld, int64_t batch,
                               int64_t src_bs, int64_t dst_bs) {
+  pdl_launch_dependents();
+  pdl_wait();
   using T = typename std::conditional<
       G == 16, uint4,
       typename std::conditional<G == 8, uint2,
@@ -109,13 +111,10 @@ mm_status repack(const void *src, void *dst, int64_t rows, int64_t row_bytes, in
   if (blocks < 1) blocks = 1;
   const char *sp = static_cast<const char *>(src);
   char *dp = static_cast<char *>(dst);
-  switch (g) {
-  case 16: repack_kernel<16><<<blocks, 256, 0, s>>>(sp, dp, rows, row_bytes, src_ld, dst_ld, batch, src_bs, dst_bs); break;
-  case 8: repack_kernel<8><<<blocks, 256, 0, s>>>(sp, dp, rows, row_bytes, src_ld, dst_ld, batch, src_bs, dst_bs); break;
-  case 4: repack_kernel<4><<<blocks, 256, 0, s>>>(sp, dp, rows, row_bytes, src_ld, dst_ld, batch, src_bs, dst_bs); break;
-  default: repack_kernel<2><<<blocks, 256, 0, s>>>(sp, dp, rows, row_bytes, src_ld, dst_ld, batch, src_bs, dst_bs); break;
-  }
-  cudaError_t e = cudaGetLastError();
+  auto kern = g == 16 ? repack_kernel<16> : g == 8 ? repack_kernel<8> : g == 4 ? repack_kernel<4>
+                                                                           : repack_kernel<2>;
+  cudaError_t e = launch_pdl(kern, dim3(blocks), dim3(256), 0, s, dim3(1), sp, dp, rows, row_bytes,
+                             src_ld, dst_ld, batch, src_bs, dst_bs);
   return e == cudaSuccess ? MM_OK : cuda_error(e, "repack_kernel launch");
 }
 

@@ -66,6 +66,9 @@ struct TcParams {
   // MN-major operand whose boxes of one stage come from a single 4-D copy
   // (map over (atom, K, atom index, batch)); 0: one 3-D copy per box
   int a_4d, b_4d;
+  // output stored transposed: element (i, j) of the computed product goes to
+  // C[j * ldc + i] (the swapped form C^T = B^T A^T of a product with small M)
+  int c_trans;
   uint64_t timeout_ns;
   // 2-SM kernel: units [0, full_units) are whole tiles; the remaining tiles
   // of the last partial wave are split along N into two half-width units
@@ -261,6 +264,15 @@ __device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
   return *reinterpret_cast<uint32_t *>(&v);
 }
 
+__device__ __forceinline__ void store_one(void *C, int tc, int64_t off, float v) {
+  if (tc == MM_F32)
+    static_cast<float *>(C)[off] = v;
+  else if (tc == MM_BF16)
+    static_cast<__nv_bfloat16 *>(C)[off] = __float2bfloat16_rn(v);
+  else
+    static_cast<__half *>(C)[off] = __float2half_rn(v);
+}
+
 __device__ __forceinline__ void store_chunk(const TcParams &p, int b, int sp, int row, int col0,
                                             const uint32_t (&r)[32]) {
   if (row >= p.M) return;
@@ -277,6 +289,13 @@ __device__ __forceinline__ void store_chunk(const TcParams &p, int b, int sp, in
       for (int i = 0; i < 32; ++i)
         if (col0 + i < p.N) dst[i] = __uint_as_float(r[i]);
     }
+    return;
+  }
+  if (p.c_trans) {
+    for (int i = 0; i < 32; ++i)
+      if (col0 + i < p.N)
+        store_one(p.C, p.tc, (int64_t)b * p.sC + (int64_t)(col0 + i) * p.ldc + row,
+                  __uint_as_float(r[i]));
     return;
   }
   const int64_t off = (int64_t)b * p.sC + (int64_t)row * p.ldc + col0;
@@ -337,6 +356,7 @@ template <int BN, int STAGES, int ES>
 __global__ void __launch_bounds__(kTcThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const TcParams p) {
+  pdl_launch_dependents();
   constexpr uint32_t A_BYTES = BM * 128;
   constexpr uint32_t B_BYTES = BN * 128;
   constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
@@ -385,6 +405,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  pdl_wait();  // the prologue above touched no global memory
 
   if (warp == 0 || warp == 6) {
     // ------------------------------------------------------------ TMA producers
@@ -691,6 +712,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     tc2_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                     const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmBh, const TcParams p) {
+  pdl_launch_dependents();
   constexpr int BNH = BN / 2;                 // B columns held by each CTA
   constexpr uint32_t A_BYTES = BM * 128;
   constexpr uint32_t B_BYTES = BNH * 128;
@@ -750,6 +772,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const uint32_t tmem_base = *tmem_slot;
   const uint32_t leader_full0 = map_to_rank(full0, rank & ~1u);
   const uint32_t leader_tempty0 = map_to_rank(tempty0, rank & ~1u);
+  pdl_wait();  // the prologue above touched no global memory
 
   if (warp == 0 || warp == 6) {
     // ------------------------------------------------------------ TMA producers (both CTAs)
@@ -922,7 +945,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
 // Sum the split-K partials in increasing slice order and convert.
 __global__ void splitk_reduce_kernel(const float *__restrict__ ws, int S, int batch, int M, int N,
-                                     void *C, int tc, int64_t ldc, int64_t sC) {
+                                     void *C, int tc, int64_t ldc, int64_t sC, int c_trans) {
+  pdl_launch_dependents();
+  pdl_wait();
   const int64_t MN = (int64_t)M * N;
   const int64_t total = (int64_t)batch * MN;
   const int64_t SBMN = (int64_t)batch * MN;
@@ -931,13 +956,7 @@ __global__ void splitk_reduce_kernel(const float *__restrict__ ws, int S, int ba
     float sum = 0.f;
     for (int s = 0; s < S; ++s) sum += __ldcs(ws + s * SBMN + e);
     const int64_t b = e / MN, rem = e - b * MN, i = rem / N, j = rem - i * N;
-    const int64_t off = b * sC + i * ldc + j;
-    if (tc == MM_F32)
-      static_cast<float *>(C)[off] = sum;
-    else if (tc == MM_BF16)
-      static_cast<__nv_bfloat16 *>(C)[off] = __float2bfloat16_rn(sum);
-    else
-      static_cast<__half *>(C)[off] = __float2half_rn(sum);
+    store_one(C, tc, c_trans ? b * sC + j * ldc + i : b * sC + i * ldc + j, sum);
   }
 }
 
@@ -951,15 +970,18 @@ struct TcCfg {
   int cl;       // pairs per cluster (2: two pairs along N share A by multicast)
 };
 
+// In the tuner's priority order: where a round ends early (a candidate within
+// the roofline limit), the earlier entry wins, so the configurations that are
+// fastest on large problems come first.
 const TcCfg kCfgs[] = {
+    {"tc2_256x256_s7", 256, 7, false, true, 1},
+    {"tc2x2_256x256_s7", 256, 7, false, true, 2},
+    {"tc2_256x128_s8", 128, 8, false, true, 1},
     {"tc_128x256_s4", 256, 4, false, false, 1},
     {"tc_128x128_s6", 128, 6, false, false, 1},
     {"tc_128x64_s8", 64, 8, false, false, 1},
     {"tc_splitk_128x128_s6", 128, 6, true, false, 1},
     {"tc_splitk_128x64_s8", 64, 8, true, false, 1},
-    {"tc2_256x256_s7", 256, 7, false, true, 1},
-    {"tc2_256x128_s8", 128, 8, false, true, 1},
-    {"tc2x2_256x256_s7", 256, 7, false, true, 2},
 };
 
 size_t smem_bytes(int bn, int stages) {
@@ -1054,8 +1076,8 @@ mm_status launch_kernel(const CUtensorMap &ma, const CUtensorMap &mb, const TcPa
                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   });
   if (attr_err != cudaSuccess) return cuda_error(attr_err, "cudaFuncSetAttribute (tc smem)");
-  tc_gemm_kernel<BN, STAGES, ES><<<grid, kTcThreads, smem, s>>>(ma, mb, tp);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(tc_gemm_kernel<BN, STAGES, ES>, dim3(grid), dim3(kTcThreads), smem, s,
+                             dim3(1), ma, mb, tp);
   if (e != cudaSuccess) return cuda_error(e, "tc_gemm_kernel launch");
   return MM_OK;
 }
@@ -1101,10 +1123,9 @@ struct PairKernel {
   }
   static mm_status launch(const CUtensorMap &ma, const CUtensorMap &mb, const CUtensorMap &mbh,
                           const TcParams &tp, int clusters, cudaStream_t s) {
-    cudaLaunchAttribute attr[1];
-    cudaLaunchConfig_t lc = config(smem(), s, attr);
-    lc.gridDim = dim3((unsigned)(2 * CL * clusters));
-    cudaError_t e = cudaLaunchKernelEx(&lc, tc2_gemm_kernel<BN, STAGES, ES, CL>, ma, mb, mbh, tp);
+    cudaError_t e = launch_pdl(tc2_gemm_kernel<BN, STAGES, ES, CL>,
+                               dim3((unsigned)(2 * CL * clusters)), dim3(kTcThreads), smem(), s,
+                               dim3(2 * CL), ma, mb, mbh, tp);
     if (e != cudaSuccess) return cuda_error(e, "tc2_gemm_kernel launch");
     return MM_OK;
   }
@@ -1231,9 +1252,8 @@ mm_status launch_tc_splitk_into(const Problem &p, const DeviceInfo &di, int cfg,
   if (st != MM_OK) return st;
   const int64_t total = (int64_t)tp.batch * p.M * p.N;
   int blocks = (int)std::min<int64_t>(ceil_div(total, 256), (int64_t)di.sms * 8);
-  splitk_reduce_kernel<<<blocks, 256, 0, s>>>(tp.ws, tp.splits, tp.batch, tp.M, tp.N, p.C, p.tc,
-                                               p.ldc, p.sC);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(splitk_reduce_kernel, dim3(blocks), dim3(256), 0, s, dim3(1), tp.ws,
+                             tp.splits, tp.batch, tp.M, tp.N, p.C, p.tc, p.ldc, p.sC, 0);
   if (e != cudaSuccess) return cuda_error(e, "splitk_reduce_kernel launch");
   return MM_OK;
 }
@@ -1279,7 +1299,43 @@ bool tc_supports(const Problem &p, const DeviceInfo &d, int cfg, std::string *wh
   return true;
 }
 
+namespace {
+mm_status launch_tc_impl(const Problem &p, LaunchCtx &ctx, int cfg, bool c_trans);
+}
+
 mm_status launch_tc(const Problem &p, LaunchCtx &ctx, int cfg) {
+  return launch_tc_impl(p, ctx, cfg, false);
+}
+
+// C^T = B^T A^T: the problem with the operands exchanged and M, N swapped;
+// C keeps its place and is written transposed.
+Problem swap_problem(const Problem &p) {
+  Problem q = p;
+  q.A = p.B;
+  q.ta = p.tb;
+  q.at = !p.bt;
+  q.lda = p.ldb;
+  q.sA = p.sB;
+  q.B = p.A;
+  q.tb = p.ta;
+  q.bt = !p.at;
+  q.ldb = p.lda;
+  q.sB = p.sA;
+  q.M = p.N;
+  q.N = p.M;
+  return q;
+}
+
+bool tc_swap_supports(const Problem &p, const DeviceInfo &d, int cfg, std::string *why) {
+  return tc_supports(swap_problem(p), d, cfg, why);
+}
+
+mm_status launch_tc_swapped(const Problem &p, LaunchCtx &ctx, int cfg) {
+  return launch_tc_impl(swap_problem(p), ctx, cfg, true);
+}
+
+namespace {
+mm_status launch_tc_impl(const Problem &p, LaunchCtx &ctx, int cfg, bool c_trans) {
   std::string why;
   if (!tc_supports(p, ctx.dev->info, cfg, &why))
     return set_error(MM_ERR_UNSUPPORTED, "%s: %s", kCfgs[cfg].name, why.c_str());
@@ -1325,6 +1381,7 @@ mm_status launch_tc(const Problem &p, LaunchCtx &ctx, int cfg) {
   std::memset(&tp, 0, sizeof tp);
   tp.a_4d = a_4d ? 1 : 0;
   tp.b_4d = b_4d ? 1 : 0;
+  tp.c_trans = c_trans ? 1 : 0;
   tp.M = (int)p.M;
   tp.N = (int)p.N;
   tp.K = (int)p.K;
@@ -1411,12 +1468,14 @@ mm_status launch_tc(const Problem &p, LaunchCtx &ctx, int cfg) {
   if (tp.splits > 1) {
     const int64_t total = (int64_t)tp.batch * p.M * p.N;
     int blocks = (int)std::min<int64_t>(ceil_div(total, 256), (int64_t)ctx.dev->info.sms * 8);
-    splitk_reduce_kernel<<<blocks, 256, 0, ctx.stream>>>(tp.ws, tp.splits, tp.batch, tp.M, tp.N,
-                                                         p.C, p.tc, p.ldc, p.sC);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(splitk_reduce_kernel, dim3(blocks), dim3(256), 0, ctx.stream, dim3(1),
+                               tp.ws, tp.splits, tp.batch, tp.M, tp.N, p.C, p.tc, p.ldc, p.sC,
+                               tp.c_trans);
     if (e != cudaSuccess) return cuda_error(e, "splitk_reduce_kernel launch");
   }
   return MM_OK;
 }
+
+}  // namespace
 
 }  // namespace mm

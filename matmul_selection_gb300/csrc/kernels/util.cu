@@ -14,11 +14,15 @@ namespace mm {
 namespace {
 
 __global__ void empty_kernel(int *p) {
+  pdl_launch_dependents();
+  pdl_wait();
   if (p && blockIdx.x == 0 && threadIdx.x == 0) *p = 0;
 }
 
 // Grid-stride 16-byte writes over a buffer larger than L2, evicting it.
 __global__ void flush_kernel(uint4 *buf, size_t n16, unsigned seed) {
+  pdl_launch_dependents();
+  pdl_wait();
   size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
   size_t stride = (size_t)gridDim.x * blockDim.x;
   for (; i < n16; i += stride) buf[i] = make_uint4(seed, (unsigned)i, seed, (unsigned)i);
@@ -26,6 +30,8 @@ __global__ void flush_kernel(uint4 *buf, size_t n16, unsigned seed) {
 
 // Grid-stride 16-byte copy: the bandwidth probe.
 __global__ void copy_kernel(const uint4 *__restrict__ src, uint4 *__restrict__ dst, size_t n16) {
+  pdl_launch_dependents();
+  pdl_wait();
   size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
   size_t stride = (size_t)gridDim.x * blockDim.x;
   for (; i < n16; i += stride) dst[i] = src[i];
@@ -34,6 +40,8 @@ __global__ void copy_kernel(const uint4 *__restrict__ src, uint4 *__restrict__ d
 // Occupies the stream for about `ns` nanoseconds (one thread, bounded by
 // %globaltimer), so that work enqueued behind it meanwhile runs back to back.
 __global__ void delay_kernel(unsigned long long ns) {
+  pdl_launch_dependents();
+  pdl_wait();
   unsigned long long t0;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
   unsigned long long t = t0;
@@ -53,6 +61,8 @@ __device__ __forceinline__ float ld_any(const void *p, int64_t i, int t) {
 __global__ void compare_kernel(const void *x, const void *ref, int t, int64_t rows, int64_t cols,
                                int64_t ld, int64_t batch, int64_t bstride, float atol, float rtol,
                                int *bad) {
+  pdl_launch_dependents();
+  pdl_wait();
   int64_t total = rows * cols * batch;
   for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total;
        e += (int64_t)gridDim.x * blockDim.x) {
@@ -66,39 +76,35 @@ __global__ void compare_kernel(const void *x, const void *ref, int t, int64_t ro
 }  // namespace
 
 mm_status launch_empty(cudaStream_t s) {
-  empty_kernel<<<1, 32, 0, s>>>(nullptr);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(empty_kernel, dim3(1), dim3(32), 0, s, dim3(1), (int *)nullptr);
   return e == cudaSuccess ? MM_OK : cuda_error(e, "empty_kernel launch");
 }
 
 mm_status launch_delay(unsigned long long ns, cudaStream_t s) {
   if (ns > 10000000ull) ns = 10000000ull;  // never more than 10 ms
-  delay_kernel<<<1, 1, 0, s>>>(ns);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(delay_kernel, dim3(1), dim3(1), 0, s, dim3(1), ns);
   return e == cudaSuccess ? MM_OK : cuda_error(e, "delay_kernel launch");
 }
 
 mm_status launch_l2_flush(void *buf, size_t bytes, cudaStream_t s) {
   static unsigned seed = 1;
   size_t n16 = bytes / 16;
-  flush_kernel<<<1024, 256, 0, s>>>(static_cast<uint4 *>(buf), n16, seed++);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(flush_kernel, dim3(1024), dim3(256), 0, s, dim3(1),
+                             static_cast<uint4 *>(buf), n16, seed++);
   return e == cudaSuccess ? MM_OK : cuda_error(e, "flush_kernel launch");
 }
 
 mm_status launch_copy_probe(const void *src, void *dst, size_t bytes, cudaStream_t s) {
-  copy_kernel<<<2048, 256, 0, s>>>(static_cast<const uint4 *>(src), static_cast<uint4 *>(dst),
-                                   bytes / 16);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(copy_kernel, dim3(2048), dim3(256), 0, s, dim3(1),
+                             static_cast<const uint4 *>(src), static_cast<uint4 *>(dst), bytes / 16);
   return e == cudaSuccess ? MM_OK : cuda_error(e, "copy_kernel launch");
 }
 
 mm_status launch_compare(const void *x, const void *ref, int dtype, int64_t rows, int64_t cols,
                          int64_t ld, int64_t batch, int64_t bstride, double atol, double rtol,
                          int *d_bad, cudaStream_t s) {
-  compare_kernel<<<1024, 256, 0, s>>>(x, ref, dtype, rows, cols, ld, batch, bstride, (float)atol,
-                                      (float)rtol, d_bad);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(compare_kernel, dim3(1024), dim3(256), 0, s, dim3(1), x, ref, dtype,
+                             rows, cols, ld, batch, bstride, (float)atol, (float)rtol, d_bad);
   return e == cudaSuccess ? MM_OK : cuda_error(e, "compare_kernel launch");
 }
 

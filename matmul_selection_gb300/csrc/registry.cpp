@@ -53,6 +53,16 @@ std::vector<Candidate> build_registry() {
   for (int i = 0; i < repack_config_count(); ++i)
     r.push_back({repack_config_name(i), GROUP_TENSOR, i, prio_repack, repack_supports,
                  launch_repack});
+  // small-M products on the tensor cores: C^T = B^T A^T puts M on the tile's
+  // N side (zero-padded to 64) and the long N on its 128-row side; split-K
+  // spreads the single row of tiles over the SMs
+  const struct {
+    const char *name, *cfg;
+  } swaps[] = {{"gemv_swap_tc_splitk_128x64_s8", "tc_splitk_128x64_s8"},
+               {"gemv_swap_tc_128x64_s8", "tc_128x64_s8"}};
+  for (const auto &sw : swaps)
+    r.push_back({sw.name, GROUP_GEMV, tc_config_index(sw.cfg), prio_gemv, tc_swap_supports,
+                 launch_tc_swapped});
   return r;
 }
 
