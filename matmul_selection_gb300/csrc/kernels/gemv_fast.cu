@@ -15,9 +15,22 @@
 //       summed in a fixed order: the two rows of a warp by shuffle, the 16 warps
 //       through shared memory, then the 8 CTAs through distributed shared
 //       memory, rank 0..7 in order, each rank finishing CW/8 of the columns.
+//   gemv_n_stream  M = 1, B row-major [K][N], no clusters.  CTA (g, s) covers the
+//       256-byte column group g of the K rows [s*KS, (s+1)*KS), about 256
+//       CTAs in all.  Before the grid waits for its predecessor, each CTA
+//       prefetches its rows of the group into L2 (cp.async.bulk.prefetch.L2):
+//       a prefetch returns nothing to the SM, so it cannot observe a stale
+//       value (the loads after the wait read the coherent L2), and back-to-back
+//       launches keep HBM busy across the kernel boundary.  A clustered grid
+//       cannot start early this way (a cluster needs its GPC's slots free at
+//       once), hence the split sums go to an fp32 workspace and a second,
+//       small kernel adds them in split order (a ticketed last-CTA sum in the
+//       same kernel put ~2 us of serial fence/atomic/reload latency on every
+//       launch's critical path).
 //   gemv_t_rows  B transposed [N][K].  One warp per output column (row of B)
 //       reading the whole row with 16-byte loads; the dot products end in an
-//       xor-shuffle reduction.  No cross-warp or cross-CTA combination.
+//       xor-shuffle reduction.  No cross-warp or cross-CTA combination.  The
+//       rows are prefetched into L2 before the wait, as above.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -102,8 +115,16 @@ struct FastArgs {
   int tc;
   int64_t ldc, sC;
   int M, N, K, batch;
-  int KS;  // gemv_n_cluster: rows per cluster rank
+  int KS;  // gemv_n_cluster: rows per cluster rank; gemv_n_stream: rows per split
+  // gemv_n_stream
+  int G, S;           // column groups, K splits
+  float *ws;          // [batch][G][S][MT][CW] split sums
 };
+
+// Warm L2 with `bytes` (a multiple of 16) at a 16-byte aligned address.
+__device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
 
 // Stage n_elems elements of A (index -> (m, k) by `map`) into smem as fp32,
 // loads batched 8 at a time so their latencies overlap.
@@ -257,11 +278,167 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1) gemv_n_cluster_kern
   asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
 }
 
+// ---------------------------------------------------------------- gemv_n_stream
+// 512 threads with 8 loads in flight a lane (two CTAs an SM): the bytes in
+// flight, not the arithmetic, bound a single pass over B.  With K split the
+// CTAs only write their partial sums; a second small kernel adds them (its
+// launch overlaps this grid's tail, and the next pass over B may start its
+// prefetch while it runs).
+constexpr int kStreamThreads = 512;
+constexpr int kStreamWarps = kStreamThreads / 32;
+
+template <int MT, int TB>
+__global__ void __launch_bounds__(kStreamThreads, 2) gemv_n_stream_kernel(const FastArgs g) {
+  pdl_launch_dependents();
+  constexpr int EB = TB == MM_F32 ? 4 : 2;
+  constexpr int VEC = 16 / EB;
+  constexpr int CW = 256 / EB;          // columns per group: 256 bytes of a row
+  constexpr int LPR = CW / VEC;         // 16 lanes per row segment
+  constexpr int RPW = 32 / LPR;         // 2 rows per warp instruction
+  constexpr int STEP = kStreamWarps * RPW;    // 32 rows per step
+  constexpr int U = 8;                  // loads in flight per lane
+  constexpr int APT = MT;               // A elements a thread preloads (slices of <= 512 rows)
+  extern __shared__ float fsm[];
+  float *As = fsm;                      // [KS][MT]
+  float *part = fsm + g.KS * MT;        // [warps][MT][CW]
+  const int grp = blockIdx.x, sp = blockIdx.y, b = blockIdx.z;
+  const int k0 = sp * g.KS;
+  const int kr = max(0, min(g.KS, g.K - k0));
+  const char *Bb = g.B + (int64_t)b * g.sB * EB;
+  {  // this CTA's rows of the column group, whole 16-byte pieces
+    const int64_t run = ((int64_t)min(CW, g.N - grp * CW) * EB) & ~(int64_t)15;
+    if (run > 0)
+      for (int r = threadIdx.x; r < kr; r += kStreamThreads)
+        prefetch_l2(Bb + ((int64_t)(k0 + r) * g.ldb + (int64_t)grp * CW) * EB, (uint32_t)run);
+  }
+  pdl_wait();  // A, the workspace and C only after the previous kernel completed
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int sub = lane / LPR, li = lane % LPR;
+  const int col = grp * CW + li * VEC;
+  // this thread's elements of A's slice: issued first, stored after B's first loads
+  const int na = g.KS * MT;
+  float areg[APT];
+#pragma unroll
+  for (int u = 0; u < APT; ++u) {
+    const int e = threadIdx.x + u * kStreamThreads;
+    const int kk = e / MT, m = e - kk * MT;
+    areg[u] = (e < na && m < g.M && kk < kr)
+                  ? ld_any(g.A, (int64_t)b * g.sA + (int64_t)m * g.a_rs + (int64_t)(k0 + kk) * g.a_cs,
+                           g.ta)
+                  : 0.f;
+  }
+  float acc[MT][VEC];
+#pragma unroll
+  for (int m = 0; m < MT; ++m)
+#pragma unroll
+    for (int j = 0; j < VEC; ++j) acc[m][j] = 0.f;
+  bool staged = false;
+  for (int r0 = warp * RPW + sub; r0 < g.KS; r0 += STEP * U) {
+    uint4 v[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int r = r0 + u * STEP;
+      v[u] = (r < kr) ? load16<TB>(Bb + (int64_t)(k0 + r) * g.ldb * EB, col, g.N)
+                      : make_uint4(0, 0, 0, 0);
+    }
+    if (!staged) {  // B's first loads are in flight; now publish A's slice
+#pragma unroll
+      for (int u = 0; u < APT; ++u) {
+        const int e = threadIdx.x + u * kStreamThreads;
+        if (e < na) As[e] = areg[u];
+      }
+      for (int e = threadIdx.x + APT * kStreamThreads; e < na; e += kStreamThreads) {  // slices > 512 rows
+        const int kk = e / MT, m = e - kk * MT;
+        As[e] = (m < g.M && kk < kr) ? ld_any(g.A, (int64_t)b * g.sA + (int64_t)m * g.a_rs +
+                                                       (int64_t)(k0 + kk) * g.a_cs, g.ta)
+                                     : 0.f;
+      }
+      __syncthreads();
+      staged = true;
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int r = r0 + u * STEP;
+      if (r < kr) {
+        float bf[VEC];
+        unpack16<TB>(v[u], bf);
+        const float *a = As + r * MT;
+#pragma unroll
+        for (int m = 0; m < MT; ++m)
+#pragma unroll
+          for (int j = 0; j < VEC; ++j) acc[m][j] = fmaf(a[m], bf[j], acc[m][j]);
+      }
+    }
+  }
+  // rows of a warp: fixed-order xor shuffle over the RPW row lanes
+#pragma unroll
+  for (int m = 0; m < MT; ++m)
+#pragma unroll
+    for (int j = 0; j < VEC; ++j) {
+      float x = acc[m][j];
+#pragma unroll
+      for (int o = LPR; o < 32; o <<= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+      acc[m][j] = x;
+    }
+  if (sub == 0)
+#pragma unroll
+    for (int m = 0; m < MT; ++m)
+#pragma unroll
+      for (int j = 0; j < VEC; ++j) part[(warp * MT + m) * CW + li * VEC + j] = acc[m][j];
+  __syncthreads();
+  // the CTA's sum over its warps in order
+  constexpr int PER = (MT * CW + kStreamThreads - 1) / kStreamThreads;
+  float cta[PER];
+#pragma unroll
+  for (int q = 0; q < PER; ++q) {
+    const int e = threadIdx.x + q * kStreamThreads;
+    float t = 0.f;
+    if (e < MT * CW)
+      for (int w = 0; w < kStreamWarps; ++w) t += part[w * MT * CW + e];
+    cta[q] = t;
+  }
+  if (g.S == 1) {
+#pragma unroll
+    for (int q = 0; q < PER; ++q) {
+      const int e = threadIdx.x + q * kStreamThreads;
+      const int m = e / CW, n = grp * CW + (e - m * CW);
+      if (e < MT * CW && m < g.M && n < g.N)
+        st_any(g.C, (int64_t)b * g.sC + (int64_t)m * g.ldc + n, g.tc, cta[q]);
+    }
+    return;
+  }
+  float *ws_part = g.ws + (((int64_t)b * g.G + grp) * g.S + sp) * (MT * CW);
+#pragma unroll
+  for (int q = 0; q < PER; ++q) {
+    const int e = threadIdx.x + q * kStreamThreads;
+    if (e < MT * CW) __stcg(ws_part + e, cta[q]);
+  }
+}
+
+// The split sums of gemv_n_stream, added in split order: one thread per
+// output element.
+template <int MT, int CW>
+__global__ void __launch_bounds__(256) gemv_stream_reduce_kernel(const FastArgs g) {
+  pdl_launch_dependents();
+  pdl_wait();
+  const int64_t total = (int64_t)g.batch * g.G * MT * CW;
+  for (int64_t x = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; x < total;
+       x += (int64_t)gridDim.x * blockDim.x) {
+    const int e = (int)(x % (MT * CW));
+    const int64_t tile = x / (MT * CW);  // b * G + grp
+    const int grp = (int)(tile % g.G), b = (int)(tile / g.G);
+    const int m = e / CW, n = grp * CW + (e - m * CW);
+    const float *p = g.ws + tile * g.S * (MT * CW) + e;
+    float t = 0.f;
+    for (int q = 0; q < g.S; ++q) t += __ldcg(p + (int64_t)q * MT * CW);
+    if (m < g.M && n < g.N) st_any(g.C, (int64_t)b * g.sC + (int64_t)m * g.ldc + n, g.tc, t);
+  }
+}
+
 // ---------------------------------------------------------------- gemv_t_rows
 template <int MT, int TB>
 __global__ void __launch_bounds__(kThreads, MT <= 2 ? 2 : 1) gemv_t_rows_kernel(const FastArgs g) {
   pdl_launch_dependents();
-  pdl_wait();
   constexpr int EB = TB == MM_F32 ? 4 : 2;
   constexpr int VEC = 16 / EB;
   constexpr int U = 8;
@@ -272,6 +449,12 @@ __global__ void __launch_bounds__(kThreads, MT <= 2 ? 2 : 1) gemv_t_rows_kernel(
   const int n = blockIdx.x * kWarps + warp;
   const char *row = g.B + ((int64_t)b * g.sB + (int64_t)min(n, g.N - 1) * g.ldb) * EB;
   const bool valid = n < g.N;
+  if (valid) {  // this warp's row of B, in whole 16-byte pieces of at most 4 KB
+    const int64_t bytes = ((int64_t)g.K * EB) & ~(int64_t)15;
+    for (int64_t o = (int64_t)lane * 4096; o < bytes; o += 32 * 4096)
+      prefetch_l2(row + o, (uint32_t)min((int64_t)4096, bytes - o));
+  }
+  pdl_wait();
   float acc[MT];
 #pragma unroll
   for (int m = 0; m < MT; ++m) acc[m] = 0.f;
@@ -325,8 +508,28 @@ __global__ void __launch_bounds__(kThreads, MT <= 2 ? 2 : 1) gemv_t_rows_kernel(
 struct FastCfg {
   const char *name;
   bool b_trans;
+  bool stream;  // gemv_n_stream
 };
-const FastCfg kFastCfgs[] = {{"gemv_n_cluster", false}, {"gemv_t_rows", true}};
+const FastCfg kFastCfgs[] = {
+    {"gemv_n_cluster", false, false}, {"gemv_t_rows", true, false}, {"gemv_n_stream", false, true}};
+
+constexpr int kStreamMaxM = 1;
+constexpr int kStreamMaxRows = 2048;
+constexpr int64_t kStreamTargetCtas = 256;
+
+// gemv_n_stream geometry: column groups, K splits and rows per split so that
+// the grid holds about kStreamTargetCtas CTAs.
+void stream_plan(int64_t N, int64_t K, int64_t batch, int eb, int64_t *G, int64_t *S, int *KS) {
+  const int64_t cw = 256 / eb;
+  *G = (N + cw - 1) / cw;
+  int64_t s = (kStreamTargetCtas + *G * batch - 1) / (*G * batch);
+  if (s < 1) s = 1;
+  int64_t ks = (K + s - 1) / s;
+  ks = (ks + 31) / 32 * 32;
+  if (ks > kStreamMaxRows) ks = kStreamMaxRows;
+  *KS = (int)ks;
+  *S = (K + ks - 1) / ks;
+}
 
 int mt_of(int64_t M) { return M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : 8; }
 
@@ -337,6 +540,9 @@ size_t smem_n(int mt, int ks, int eb) {
   return ((size_t)ks * mt + (size_t)kWarps * mt * (256 / eb)) * sizeof(float);
 }
 size_t smem_t(int mt, int64_t K) { return (size_t)mt * K * sizeof(float); }
+size_t smem_stream(int mt, int ks, int eb) {
+  return ((size_t)ks * mt + (size_t)kStreamWarps * mt * (256 / eb)) * sizeof(float);
+}
 
 int rows_per_rank(int64_t K) {
   int64_t ks = (K + kCluster - 1) / kCluster;
@@ -375,6 +581,28 @@ mm_status launch_t(const FastArgs &g, size_t smem, cudaStream_t s) {
   return e == cudaSuccess ? MM_OK : cuda_error(e, "gemv_t_rows launch");
 }
 
+template <int MT, int TB>
+mm_status launch_stream(const FastArgs &g, size_t smem, cudaStream_t s) {
+  auto kern = gemv_n_stream_kernel<MT, TB>;
+  cudaError_t e;
+  e = smem_attr(kern, smem);
+  if (e != cudaSuccess) return cuda_error(e, "gemv_n_stream smem attribute");
+  e = launch_pdl(kern, dim3((unsigned)g.G, (unsigned)g.S, (unsigned)g.batch), dim3(kStreamThreads),
+                 smem, s, dim3(1), g);
+  if (e != cudaSuccess) return cuda_error(e, "gemv_n_stream launch");
+  if (g.S == 1) return MM_OK;
+  constexpr int CW = TB == MM_F32 ? 64 : 128;
+  const int64_t total = (int64_t)g.batch * g.G * MT * CW;
+  const int blocks = (int)std::min<int64_t>((total + 255) / 256, 4096);
+  e = launch_pdl(gemv_stream_reduce_kernel<MT, CW>, dim3(blocks), dim3(256), 0, s, dim3(1), g);
+  return e == cudaSuccess ? MM_OK : cuda_error(e, "gemv_stream_reduce launch");
+}
+
+template <int TB>
+mm_status launch_stream_tb(int, const FastArgs &g, size_t smem, cudaStream_t s) {
+  return launch_stream<1, TB>(g, smem, s);
+}
+
 template <int TB>
 mm_status launch_tb(bool bt, int mt, const FastArgs &g, int groups, size_t smem, cudaStream_t s) {
   switch (mt) {
@@ -406,7 +634,17 @@ bool gemv_fast_supports(const Problem &p, const DeviceInfo &d, int cfg, std::str
   if ((p.ldb * eb) % 16) return no("ldb not a multiple of 16 bytes");
   if (p.batch > 1 && (p.sB * eb) % 16) return no("B batch stride not a multiple of 16 bytes");
   const int mt = mt_of(p.M);
-  size_t smem = c.b_trans ? smem_t(mt, p.K) : smem_n(mt, rows_per_rank(p.K), eb);
+  size_t smem;
+  if (c.stream) {
+    if (p.M > kStreamMaxM) return no("M must be 1");
+    int64_t G, S;
+    int KS;
+    stream_plan(p.N, p.K, p.batch, eb, &G, &S, &KS);
+    if (G >= (1LL << 31) || S > 65535) return no("too many column groups or splits");
+    smem = smem_stream(mt, KS, eb);
+  } else {
+    smem = c.b_trans ? smem_t(mt, p.K) : smem_n(mt, rows_per_rank(p.K), eb);
+  }
   if (smem > kMaxSmem || (int64_t)smem > d.smem_optin) return no("A slice too large for shared memory");
   return true;
 }
@@ -437,6 +675,24 @@ mm_status launch_gemv_fast(const Problem &p, LaunchCtx &ctx, int cfg) {
   g.batch = (int)p.batch;
   int groups = 0;
   size_t smem;
+  if (c.stream) {
+    int64_t G, S;
+    stream_plan(p.N, p.K, p.batch, eb, &G, &S, &g.KS);
+    g.G = (int)G;
+    g.S = (int)S;
+    smem = smem_stream(mt, g.KS, eb);
+    if (S > 1) {
+      const size_t cw = 256 / eb;
+      const size_t ws_bytes = (size_t)p.batch * G * S * mt * cw * sizeof(float);
+      void *w = nullptr;
+      mm_status st = get_scratch(*ctx.dev, ctx.stream, SCRATCH_WORKSPACE, ws_bytes, &w);
+      if (st != MM_OK) return st;
+      g.ws = static_cast<float *>(w);
+    }
+    if (p.tb == MM_BF16) return launch_stream_tb<MM_BF16>(mt, g, smem, ctx.stream);
+    if (p.tb == MM_F16) return launch_stream_tb<MM_F16>(mt, g, smem, ctx.stream);
+    return launch_stream_tb<MM_F32>(mt, g, smem, ctx.stream);
+  }
   if (!c.b_trans) {
     g.KS = rows_per_rank(p.K);
     groups = (int)((p.N + 256 / eb - 1) / (256 / eb));

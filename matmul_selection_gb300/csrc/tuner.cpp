@@ -15,9 +15,13 @@
 //   * a candidate with 2 samples inside the roofline time limit short-circuits
 //     the round: no further candidate of that round is measured;
 //   * the fastest MEDIAN wins; ties go to the lower candidate index.
-// Each chunk of timed iterations is enqueued behind a short delay kernel so
-// the iterations run back to back on the device; the events then time the
-// kernels rather than the host's launch latency.
+// Iterations run in chunks (3 for the screening pass, then up to 10), each
+// enqueued behind a short delay kernel so that they run back to back on the
+// device.  A sample is the mean of a chunk, timed by one pair of events
+// around it (as TunableOp times a loop of calls): events between the calls
+// would stop a launch from overlapping its predecessor's tail, which is how
+// the library's kernels run in a stream.  With the L2 flush on, the flush
+// kernels sit between the calls, so each call is then timed on its own.
 // Every timed iteration runs on its own rotating copy of the inputs and its
 // own private output (TunableOp's rotating buffer; the page's out.copy()), so
 // the user's output is never written by tuning and repeated runs do not
@@ -38,7 +42,8 @@ namespace {
 struct CandResult {
   int index = -1;
   std::string state = "skipped";  // ok, unsupported, error, slow, timeout, numeric, skipped
-  std::vector<float> times;
+  std::vector<float> times;       // samples (ms per call)
+  int iters = 0;                  // timed calls
   double median = NAN, mean = NAN;
   bool short_circuit = false;
   std::string err;
@@ -238,23 +243,30 @@ CandResult bench_candidate(int idx, BenchEnv &env, double best_ms) {
     // hold the stream while the chunk is enqueued, so its iterations run back
     // to back and the events time the device, not the host's launch latency
     launch_delay(40000ull * (unsigned long long)chunk, ds.tune_stream);
+    const bool per_call = env.opts.l2_flush && ds.flush_buf.ptr;
+    if (!per_call) cudaEventRecord(env.ev[0], ds.tune_stream);
     for (int i = 0; i < chunk; ++i) {
       const Problem &q = env.rot->sets[(n + i) % R];
-      if (env.opts.l2_flush && ds.flush_buf.ptr) launch_l2_flush(ds.flush_buf.ptr, ds.flush_buf.bytes, ds.tune_stream);
-      cudaEventRecord(env.ev[2 * i], ds.tune_stream);
+      if (per_call) {
+        launch_l2_flush(ds.flush_buf.ptr, ds.flush_buf.bytes, ds.tune_stream);
+        cudaEventRecord(env.ev[2 * i], ds.tune_stream);
+      }
       st = launch_candidate(idx, q, ctx);
-      cudaEventRecord(env.ev[2 * i + 1], ds.tune_stream);
+      if (per_call) cudaEventRecord(env.ev[2 * i + 1], ds.tune_stream);
       if (st != MM_OK) break;
     }
+    if (!per_call) cudaEventRecord(env.ev[1], ds.tune_stream);
     ce = cudaStreamSynchronize(ds.tune_stream);
     if (st != MM_OK || ce != cudaSuccess) {
       r.state = "error";
       r.err = st != MM_OK ? std::string(mm_last_error()) : cudaGetErrorString(ce);
       return r;
     }
-    for (int i = 0; i < chunk; ++i) {
+    const int samples = per_call ? chunk : 1;
+    for (int i = 0; i < samples; ++i) {
       float ms = NAN;
       if (cudaEventElapsedTime(&ms, env.ev[2 * i], env.ev[2 * i + 1]) != cudaSuccess) ms = NAN;
+      if (!per_call) ms /= (float)chunk;
       if (faulty && env.fault.mode == "nan") ms = NAN;
       if (faulty && env.fault.mode == "slow") ms *= 1000.f;
       if (!(ms > 0) || !std::isfinite(ms)) {
@@ -263,9 +275,10 @@ CandResult bench_candidate(int idx, BenchEnv &env, double best_ms) {
         return r;
       }
       r.times.push_back(ms);
-      total += ms;
+      total += per_call ? ms : ms * chunk;
       if (ms <= env.limit_ms) ++in_limit;
     }
+    r.iters += chunk;
     n += chunk;
     if (first) {
       first = false;
@@ -334,10 +347,10 @@ void log_decision(const Options &o, const KeyPod &key, const std::vector<CandRes
     if (r.index < 0) continue;
     snprintf(b, sizeof b,
              "%s{\"index\": %d, \"name\": \"%s\", \"state\": \"%s\", \"median_ms\": %.6g, "
-             "\"mean_ms\": %.6g, \"n\": %zu%s}",
+             "\"mean_ms\": %.6g, \"n\": %d, \"samples\": %zu%s}",
              firstc ? "" : ", ", r.index, registry()[r.index].name.c_str(), state_json(r),
              std::isfinite(r.median) ? r.median : -1.0, std::isfinite(r.mean) ? r.mean : -1.0,
-             r.times.size(), r.short_circuit ? ", \"short_circuit\": true" : "");
+             r.iters, r.times.size(), r.short_circuit ? ", \"short_circuit\": true" : "");
     s += b;
     firstc = false;
   }

@@ -100,6 +100,7 @@ def test_every_candidate_runs_somewhere():
         "gemv_t": Case(4, 256, 512, layout="NT", dist="int4"),
         "gemv_n_cluster": Case(4, 1000, 520, layout="NN", dist="int4"),
         "gemv_t_rows": Case(3, 300, 1000, layout="NT", dist="int4"),
+        "gemv_n_stream": Case(1, 1000, 700, layout="NN", dist="int4"),
         "tc2_repack_256x256": Case(300, 264, 200, layout="NN", dist="int4", pad=(4, 0, 0)),
         "tc_repack_128x128": Case(300, 264, 200, layout="TN", dist="int4", pad=(3, 0, 0)),
         "tc_repack_128x64": Case(130, 72, 136, layout="NT", dist="int4", pad=(0, 5, 0)),
@@ -145,6 +146,27 @@ def test_results_deterministic():
         r1 = c.result().copy()
         assert run(i, c) == mm.MM_OK
         assert np.array_equal(r1.view(np.uint8), c.result().view(np.uint8)), NAMES[i]
+
+
+@pytest.mark.parametrize("shape", [(1, 4096, 4096), (1, 1000, 700), (1, 136, 5000), (1, 64, 33),
+                                   (1, 8, 20000)], ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("dt", [(BF16, BF16, F32), (F16, F16, F16), (F32, F32, F32)],
+                         ids=["bf16-f32", "f16-f16", "f32-f32"])
+def test_gemv_n_stream_splits(shape, dt):
+    """The split-K GEMV with a ticketed last-block sum: single and many K
+    splits, a ragged last column group, and three launches in a row (the
+    tickets must re-arm)."""
+    i = NAMES.index("gemv_n_stream")
+    c = Case(*shape, layout="NN", dt=dt, dist="int4", seed=sum(shape)).device()
+    for _ in range(3):
+        c.device()  # a fresh output each time: a ticket left armed would leave it unwritten
+        assert run(i, c) == mm.MM_OK, mm.mm_last_error()
+        c.check(exact=True)
+    # batched with gaps; B rows of 304 elements keep the 16-byte row alignment
+    cb = Case(1, 296, 900, layout="NN", dt=dt, dist="int4", batch=3, bstride_extra=(8, 16, 8),
+              pad=(8, 8, 4)).device()
+    assert run(i, cb) == mm.MM_OK, mm.mm_last_error()
+    cb.check(exact=True)
 
 
 # ---------------------------------------------------------------- full sizes
