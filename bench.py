@@ -226,31 +226,41 @@ def ensure_built():
     mod.build()
 
 
-def kernel_source(kernel_name):
-    """The source file that holds a candidate's kernel."""
+def kernel_sources(kernel_name):
+    """The source files that hold a candidate's kernels."""
     kdir = os.path.join(ROOT, "matmul_selection_gb300", "csrc", "kernels")
-    if kernel_name.startswith("tc_"):
-        return os.path.join(kdir, "tc_gemm.cu")
-    if kernel_name.startswith("gemv"):
-        return os.path.join(kdir, "gemv.cu")
-    return os.path.join(kdir, "naive.cu")
+    if kernel_name.startswith(("tc_repack", "tc2_repack")):
+        names = ["repack.cu", "tc_gemm.cu"]
+    elif kernel_name.startswith(("tc", "gemv_swap_tc")):
+        names = ["tc_gemm.cu"]
+    elif kernel_name in ("gemv_n_cluster", "gemv_t_rows", "gemv_n_stream"):
+        names = ["gemv_fast.cu"]
+    elif kernel_name.startswith("gemv"):
+        names = ["gemv.cu"]
+    else:
+        names = ["naive.cu"]
+    return [os.path.join(kdir, n) for n in names]
+
+
+def sources_sha1(kernel_name):
+    import hashlib
+    h = hashlib.sha1()
+    for path in kernel_sources(kernel_name):
+        with open(path, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:12]
 
 
 def traffic_for(kernel_name, workload):
     """DRAM bytes per launch from a committed ncu summary, or None when the
-    kernel's source changed since the counters were taken."""
-    import hashlib
+    kernel's sources changed since the counters were taken."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
     with open(path) as f:
         d = json.load(f)
     e = d.get(f"{kernel_name}@{workload}")
-    if not e:
-        return None
-    with open(kernel_source(kernel_name), "rb") as f:
-        sha = hashlib.sha1(f.read()).hexdigest()[:12]
-    if e.get("source_sha1") != sha:
+    if not e or e.get("source_sha1") != sources_sha1(kernel_name):
         return None
     return e.get("dram_bytes_per_launch")
 
