@@ -8,7 +8,9 @@
 // with its leading dimension rounded up to 16 bytes, then run a tensor-core
 // configuration on the copy.  The copy moves each misaligned operand once
 // more through HBM; for the large shapes that need it this is a few percent
-// of the product's time, against the naive kernel otherwise left.
+// of the product's time, against the naive kernel otherwise left.  The swap
+// variant (GEMV group) serves small M: it copies the few rows of A and runs
+// the split-K configuration on C^T = B^T A^T.
 #include <type_traits>
 
 #include "../common.h"
@@ -42,11 +44,13 @@ __global__ void repack_kernel(const char *__restrict__ src, char *__restrict__ d
 struct RepackCfg {
   const char *name;
   const char *inner;  // tensor-core configuration run on the copies
+  bool swap;          // run it on C^T = B^T A^T (small M: a copy of A is cheap)
 };
 const RepackCfg kRepackCfgs[] = {
-    {"tc2_repack_256x256", "tc2_256x256_s7"},
-    {"tc_repack_128x128", "tc_128x128_s6"},
-    {"tc_repack_128x64", "tc_128x64_s8"},
+    {"tc2_repack_256x256", "tc2_256x256_s7", false},
+    {"tc_repack_128x128", "tc_128x128_s6", false},
+    {"tc_repack_128x64", "tc_128x64_s8", false},
+    {"gemv_swap_tc_repack_splitk_128x64", "tc_splitk_128x64_s8", true},
 };
 
 struct Plan {
@@ -121,6 +125,7 @@ mm_status repack(const void *src, void *dst, int64_t rows, int64_t row_bytes, in
 }  // namespace
 
 int repack_config_count() { return (int)(sizeof kRepackCfgs / sizeof kRepackCfgs[0]); }
+bool repack_config_is_swap(int cfg) { return kRepackCfgs[cfg].swap; }
 const char *repack_config_name(int cfg) { return kRepackCfgs[cfg].name; }
 
 bool repack_supports(const Problem &p, const DeviceInfo &d, int cfg, std::string *why) {
@@ -141,7 +146,7 @@ bool repack_supports(const Problem &p, const DeviceInfo &d, int cfg, std::string
   static char aligned_dummy[256] __attribute__((aligned(256)));
   if (pl.a) q.A = aligned_dummy;
   if (pl.b) q.B = aligned_dummy;
-  return tc_supports(q, d, inner, why);
+  return kRepackCfgs[cfg].swap ? tc_swap_supports(q, d, inner, why) : tc_supports(q, d, inner, why);
 }
 
 mm_status launch_repack(const Problem &p, LaunchCtx &ctx, int cfg) {
@@ -173,7 +178,8 @@ mm_status launch_repack(const Problem &p, LaunchCtx &ctx, int cfg) {
     if (st != MM_OK) return st;
     q.B = base;
   }
-  return launch_tc(q, ctx, inner_index(cfg));
+  return kRepackCfgs[cfg].swap ? launch_tc_swapped(q, ctx, inner_index(cfg))
+                               : launch_tc(q, ctx, inner_index(cfg));
 }
 
 }  // namespace mm

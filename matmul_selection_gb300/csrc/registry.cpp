@@ -50,9 +50,11 @@ std::vector<Candidate> build_registry() {
                  launch_gemv_fast});
   for (int i = 0; i < tc_config_count(); ++i)
     r.push_back({tc_config_name(i), GROUP_TENSOR, i, prio_tc, tc_supports, launch_tc});
-  for (int i = 0; i < repack_config_count(); ++i)
-    r.push_back({repack_config_name(i), GROUP_TENSOR, i, prio_repack, repack_supports,
-                 launch_repack});
+  for (int i = 0; i < repack_config_count(); ++i) {
+    const bool small_m = repack_config_is_swap(i);
+    r.push_back({repack_config_name(i), small_m ? GROUP_GEMV : GROUP_TENSOR, i,
+                 small_m ? prio_gemv : prio_repack, repack_supports, launch_repack});
+  }
   // small-M products on the tensor cores: C^T = B^T A^T puts M on the tile's
   // N side (zero-padded to 64) and the long N on its 128-row side; split-K
   // spreads the single row of tiles over the SMs
