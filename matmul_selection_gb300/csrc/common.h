@@ -299,6 +299,7 @@ bool repack_supports(const Problem &p, const DeviceInfo &d, int cfg, std::string
 mm_status launch_repack(const Problem &p, LaunchCtx &ctx, int cfg);
 int repack_config_count();
 bool repack_config_is_swap(int cfg);  // a small-M (GEMV group) configuration
+bool repack_config_is_splitk(int cfg);
 const char *repack_config_name(int cfg);
 
 bool tc_supports(const Problem &p, const DeviceInfo &d, int cfg, std::string *why);

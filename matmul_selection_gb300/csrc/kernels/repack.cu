@@ -50,6 +50,8 @@ const RepackCfg kRepackCfgs[] = {
     {"tc2_repack_256x256", "tc2_256x256_s7", false},
     {"tc_repack_128x128", "tc_128x128_s6", false},
     {"tc_repack_128x64", "tc_128x64_s8", false},
+    {"tc_repack_splitk_128x128", "tc_splitk_128x128_s6", false},
+    {"tc_repack_splitk_128x64", "tc_splitk_128x64_s8", false},
     {"gemv_swap_tc_repack_splitk_128x64", "tc_splitk_128x64_s8", true},
 };
 
@@ -126,6 +128,7 @@ mm_status repack(const void *src, void *dst, int64_t rows, int64_t row_bytes, in
 
 int repack_config_count() { return (int)(sizeof kRepackCfgs / sizeof kRepackCfgs[0]); }
 bool repack_config_is_swap(int cfg) { return kRepackCfgs[cfg].swap; }
+bool repack_config_is_splitk(int cfg) { return tc_config_is_splitk(inner_index(cfg)); }
 const char *repack_config_name(int cfg) { return kRepackCfgs[cfg].name; }
 
 bool repack_supports(const Problem &p, const DeviceInfo &d, int cfg, std::string *why) {

@@ -550,13 +550,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       for (int u = blockIdx.x; u < p.total_units && ok; u += gridDim.x) {
         int tm, tn, b, sp;
         decode_unit(p, u, tm, tn, b, sp);
-        const int kb0 = sp * p.kb_per_split;
-        const int kb1 = min(p.num_kb, kb0 + p.kb_per_split);
+
         if (!warp_wait(tempty0 + 8 * acc, acc_phase ^ 1, abort_flag, p.err, kErrMma,
                        p.timeout_ns))
           break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+        const int kb0 = sp * p.kb_per_split;
+        const int kb1 = min(p.num_kb, kb0 + p.kb_per_split);
         for (int kb = kb0; kb < kb1; ++kb) {
           if (!warp_wait(full0 + 8 * stage, phase, abort_flag, p.err, kErrMma, p.timeout_ns)) {
             ok = false;
@@ -1072,14 +1073,22 @@ __global__ void splitk_reduce_kernel(const float *__restrict__ ws, int S, int ba
                                      void *C, int tc, int64_t ldc, int64_t sC, int c_trans) {
   pdl_launch_dependents();
   pdl_wait();
-  const int64_t MN = (int64_t)M * N;
-  const int64_t total = (int64_t)batch * MN;
-  const int64_t SBMN = (int64_t)batch * MN;
+  const int64_t total = (int64_t)batch * M * N;  // flattened [batch][M][N]
+  const bool narrow = total < (1LL << 32);       // 32-bit index arithmetic suffices
   for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total;
        e += (int64_t)gridDim.x * blockDim.x) {
     float sum = 0.f;
-    for (int s = 0; s < S; ++s) sum += __ldcs(ws + s * SBMN + e);
-    const int64_t b = e / MN, rem = e - b * MN, i = rem / N, j = rem - i * N;
+    for (int q = 0; q < S; ++q) sum += __ldcs(ws + q * total + e);
+    int64_t rg, j;  // row of [batch][M], column
+    if (narrow) {
+      const uint32_t r32 = (uint32_t)e / (uint32_t)N;
+      rg = r32;
+      j = (uint32_t)e - r32 * (uint32_t)N;
+    } else {
+      rg = e / N;
+      j = e - rg * N;
+    }
+    const int64_t b = batch == 1 ? 0 : rg / M, i = rg - b * M;
     store_one(C, tc, c_trans ? b * sC + j * ldc + i : b * sC + i * ldc + j, sum);
   }
 }
@@ -1283,6 +1292,13 @@ mm_status dispatch(int cfg, const CUtensorMap &ma, const CUtensorMap &mb, const 
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
+// Grid of the split-K reduction: one element a thread, about eight blocks of
+// 256 threads an SM.
+dim3 reduce_grid(const TcParams &tp, int sms) {
+  const int64_t total = (int64_t)tp.batch * tp.M * tp.N;
+  return dim3((unsigned)std::max<int64_t>(1, std::min<int64_t>(ceil_div(total, 256), (int64_t)sms * 8)));
+}
+
 // Split count for a split-K configuration: enough units to fill the SMs.
 void choose_splits(int64_t tiles, int64_t num_kb, int sms, int *splits, int *kb_per) {
   int64_t s = sms / (tiles > 0 ? tiles : 1);
@@ -1374,10 +1390,8 @@ mm_status launch_tc_splitk_into(const Problem &p, const DeviceInfo &di, int cfg,
   const int grid = (int)std::min<int64_t>(units, di.sms);
   st = es == 2 ? dispatch<2>(cfg, ma, mb, ma, tp, grid, s) : dispatch<4>(cfg, ma, mb, ma, tp, grid, s);
   if (st != MM_OK) return st;
-  const int64_t total = (int64_t)tp.batch * p.M * p.N;
-  int blocks = (int)std::min<int64_t>(ceil_div(total, 256), (int64_t)di.sms * 8);
-  cudaError_t e = launch_pdl(splitk_reduce_kernel, dim3(blocks), dim3(256), 0, s, dim3(1), tp.ws,
-                             tp.splits, tp.batch, tp.M, tp.N, p.C, p.tc, p.ldc, p.sC, 0);
+  cudaError_t e = launch_pdl(splitk_reduce_kernel, reduce_grid(tp, di.sms), dim3(256), 0, s, dim3(1),
+                             tp.ws, tp.splits, tp.batch, tp.M, tp.N, p.C, p.tc, p.ldc, p.sC, 0);
   if (e != cudaSuccess) return cuda_error(e, "splitk_reduce_kernel launch");
   return MM_OK;
 }
@@ -1599,9 +1613,8 @@ mm_status launch_tc_impl(const Problem &p, LaunchCtx &ctx, int cfg, bool c_trans
                : dispatch<4>(cfg, ma, mb, mc, tp, grid, ctx.stream);
   if (st != MM_OK) return st;
   if (tp.splits > 1) {
-    const int64_t total = (int64_t)tp.batch * p.M * p.N;
-    int blocks = (int)std::min<int64_t>(ceil_div(total, 256), (int64_t)ctx.dev->info.sms * 8);
-    cudaError_t e = launch_pdl(splitk_reduce_kernel, dim3(blocks), dim3(256), 0, ctx.stream, dim3(1),
+    cudaError_t e = launch_pdl(splitk_reduce_kernel, reduce_grid(tp, ctx.dev->info.sms), dim3(256), 0,
+                               ctx.stream, dim3(1),
                                tp.ws, tp.splits, tp.batch, tp.M, tp.N, p.C, p.tc, p.ldc, p.sC,
                                tp.c_trans);
     if (e != cudaSuccess) return cuda_error(e, "splitk_reduce_kernel launch");

@@ -27,15 +27,21 @@ namespace {
 
 int prio_naive(const KeyPod &, const Problem &, const DeviceInfo &, int) { return PRIORITY_MIN; }
 int prio_gemv(const KeyPod &, const Problem &, const DeviceInfo &, int) { return PRIORITY_HIGH; }
-int prio_tc(const KeyPod &k, const Problem &, const DeviceInfo &d, int cfg) {
-  if (!tc_config_is_splitk(cfg)) return PRIORITY_HIGH;
+// Split-K: worth measuring when 128 x 128 tiles fill at most half the SMs and
+// K is deep enough to split.
+int prio_splitk(const KeyPod &k, const DeviceInfo &d) {
   uint64_t tiles = ((k.m + 127) / 128) * ((k.n + 127) / 128) * (k.batch ? k.batch : 1);
-  uint64_t mx = k.m > k.n ? k.m : k.n;
-  if (tiles * 2 <= (uint64_t)d.sms && k.k >= 4 * mx && k.k >= 1024) return PRIORITY_HIGH;
+  if (tiles * 2 <= (uint64_t)d.sms && k.k >= 1024) return PRIORITY_HIGH;
   return PRIORITY_MIN;
 }
 
-int prio_repack(const KeyPod &, const Problem &, const DeviceInfo &, int) { return PRIORITY_HIGH; }
+int prio_tc(const KeyPod &k, const Problem &, const DeviceInfo &d, int cfg) {
+  return tc_config_is_splitk(cfg) ? prio_splitk(k, d) : PRIORITY_HIGH;
+}
+
+int prio_repack(const KeyPod &k, const Problem &, const DeviceInfo &d, int cfg) {
+  return repack_config_is_splitk(cfg) ? prio_splitk(k, d) : PRIORITY_HIGH;
+}
 
 bool naive_supports(const Problem &, const DeviceInfo &, int, std::string *) { return true; }
 mm_status naive_launch(const Problem &p, LaunchCtx &ctx, int) { return launch_naive(p, ctx.stream); }

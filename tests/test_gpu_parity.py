@@ -106,6 +106,8 @@ def test_every_candidate_runs_somewhere():
         "tc_repack_128x64": Case(130, 72, 136, layout="NT", dist="int4", pad=(0, 5, 0)),
         "gemv_swap_tc_repack_splitk_128x64": Case(16, 264, 200, layout="NN", dist="int4",
                                                   pad=(4, 0, 0)),
+        "tc_repack_splitk_128x128": Case(200, 264, 520, layout="NN", dist="int4", pad=(4, 0, 0)),
+        "tc_repack_splitk_128x64": Case(130, 72, 600, layout="TN", dist="int4", pad=(3, 0, 0)),
     }
     for i, n in enumerate(NAMES):
         c = home.get(n) or Case(256, 256, 256, layout="NN", dist="int4")
