@@ -61,7 +61,6 @@ for _m in (1, 16, 127, 1000, 4097, 8192):
             _m, 4096, 4096, "N" + _t, (BF16, BF16, BF16), "normal", "normal", 4, 1, 1004)
 
 DEFAULT_WORKLOAD = "square_4096_bf16"
-HBM_BOUND = ("gemv", "skinny", "splitk")
 
 
 def load_peaks():
@@ -412,8 +411,12 @@ def run_ours(args, w, name, rank, world, peaks, quiet=False):
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         e2e_s = float(t.item())
     e2e_value = flops * e2e_steps * world / e2e_s / 1e12
-    # roofline of the dominant (tuned) kernel
-    hbm = name.startswith(HBM_BOUND) or (w["M"] <= 16 and "bucket" in name)
+    # roofline of the dominant (tuned) kernel: the bound is whichever of the
+    # memory time (algorithmic bytes / HBM peak) and the compute time
+    # (flops / tensor peak) is longer
+    tf32 = dt[0] == F32
+    tensor_peak = peaks["bf16_tflops"] * (1.1 / 2.25 if tf32 else 1.0)
+    hbm = nbytes / (peaks["hbm_gbs"] * 1e9) > flops / (tensor_peak * 1e12)
     if hbm:
         achieved = nbytes / (kern_ms * 1e-3) / 1e9
         peak = peaks["hbm_gbs"]
@@ -422,8 +425,7 @@ def run_ours(args, w, name, rank, world, peaks, quiet=False):
                 "peak_source": peaks["source"], "algorithmic_bytes": nbytes}
     else:
         achieved = flops / (kern_ms * 1e-3) / 1e12
-        tf32 = dt[0] == F32
-        peak = peaks["bf16_tflops"] * (1.1 / 2.25 if tf32 else 1.0)
+        peak = tensor_peak
         roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak, "traffic": traffic_for(winner, name),
                 "peak_source": peaks["source"] + (" x tf32/bf16 nominal ratio" if tf32 else ""),
