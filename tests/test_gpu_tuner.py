@@ -162,12 +162,17 @@ def test_hand_edits_default_and_unknown_name(tmp_path):
 
 
 def test_tuning_disabled_runs_default():
+    """With tuning off a miss runs the plan's first supported candidate (the
+    one the tuner would measure first), records nothing and measures nothing."""
     mm.check(mm.mm_set_option("tuning", "0"))
-    c = Case(96, 80, 200, dist="int4").device()
-    n0 = mm.mm_candidate_launches(0)
-    mm.check(execute(c))
-    c.check(exact=True)
-    assert mm.mm_candidate_launches(0) == n0 + 1
+    for shape in [(96, 80, 200), (1, 512, 512), (4096, 256, 64)]:
+        c = Case(*shape, dist="int4").device()
+        items = mm.mm_plan(*shape, shape[2], shape[1], shape[1], c.dt, "NN")
+        first = next(it["cand"] for it in items if it["supported"])
+        n0 = mm.mm_candidate_launches(first)
+        mm.check(execute(c))
+        c.check(exact=True)
+        assert mm.mm_candidate_launches(first) == n0 + 1, NAMES[first]
     assert mm.mm_cache_size() == 0 and mm.mm_get_stats()["tunes"] == 0
 
 
@@ -214,6 +219,31 @@ def test_decision_log(tmp_path):
     assert rec["limit_ns"] > 0 and rec["bounds"]["compute"]["amount"] == 256 * 256 * 511
     measured = [x for x in rec["candidates"] if x["state"] == "ok"]
     assert measured and all(x["n"] >= 1 for x in measured)
+    # re-timed finalists: the recorded choice is the finalist with the lowest
+    # re-timed median, and only candidates near the first winner were re-timed
+    fin = [x for x in rec["candidates"] if "final_ms" in x]
+    if fin:
+        assert len(fin) >= 2 and len(fin) <= 3
+        best = min(fin, key=lambda x: (x["final_ms"], x["index"]))
+        assert rec["fastest_index"] == best["index"]
+        lead = min(x["median_ms"] for x in measured)
+        assert all(x["median_ms"] <= 1.10 * lead + 1e-9 for x in fin)
+
+
+def test_finalists_are_retimed(tmp_path):
+    """Two configurations of nearly equal speed (forced on the same shape)
+    give a close call; the log then carries their re-timed medians."""
+    path = str(tmp_path / "fin.jsonl")
+    mm.check(mm.mm_set_option("decisions", path))
+    c = Case(1024, 1024, 1024, dt=(BF16, BF16, BF16), dist="int4").device()
+    mm.check(execute(c))
+    c.check(exact=True)
+    rec = json.loads(open(path).read().splitlines()[-1])
+    ok = sorted((x for x in rec["candidates"] if x["state"] == "ok"), key=lambda x: x["median_ms"])
+    close = [x for x in ok if x["median_ms"] <= 1.10 * ok[0]["median_ms"]]
+    short = any(x.get("short_circuit") for x in ok)
+    if len(close) >= 2 and not short:
+        assert sum("final_ms" in x for x in rec["candidates"]) == min(3, len(close))
 
 
 def test_host_buffers_entry_point():
