@@ -162,6 +162,21 @@ mm_status mm_autotune_execute_host(const void *lhs, const void *rhs, void *out, 
  */
 mm_status mm_cache_load(const char *path);
 mm_status mm_cache_save(const char *path);
+
+/* Offline tuning (PyTorch TunableOp guide, sections 6-7: record the
+ * operations met while tuning is off, tune them later from the file).  With
+ * the option "record_untuned" set to a path (env MM_RECORD_UNTUNED), a key
+ * missed while tuning is off is appended once per process to that file as
+ *   Untuned,<key text>,M,N,K,lda,ldb,ldc,<a type>,<b type>,<c type>,<layout>,
+ *   batch,stride_a,stride_b,stride_c
+ * mm_tune_file tunes every recorded problem not yet in the current device's
+ * table, on library-allocated synthetic operands of the recorded shape and
+ * strides (freed before it returns), and sets *tuned to the number tuned;
+ * the results can then be written with mm_cache_save.  Runs whether or not
+ * the "tuning" option is on.  Errors: MM_ERR_IO if the file cannot be read,
+ * MM_ERR_INVALID_ARG for a malformed record, MM_ERR_CUDA, or the tuner's own
+ * errors; lines that are not Untuned records are skipped. */
+mm_status mm_tune_file(const char *path, int *tuned);
 /* Forget every in-memory entry of the current device. */
 mm_status mm_cache_clear(void);
 /* Number of in-memory entries of the current device (or -1 on error). */

@@ -76,6 +76,7 @@ _sig = {
                                         mm_dtypes, ctypes.c_int, ctypes.POINTER(mm_batch), _vp]),
     "mm_cache_load": (_i32, [_cp]),
     "mm_cache_save": (_i32, [_cp]),
+    "mm_tune_file": (_i32, [_cp, ctypes.POINTER(ctypes.c_int)]),
     "mm_cache_clear": (_i32, []),
     "mm_cache_size": (_i64, []),
     "mm_candidate_count": (_i32, []),
@@ -191,6 +192,14 @@ def mm_execute_candidate(index, lhs, rhs, out, M, N, K, lda, ldb, ldc, dtypes, l
 
 def mm_cache_load(path=None):
     return _lib.mm_cache_load(path.encode() if path else None)
+
+
+def mm_tune_file(path):
+    """Tune every problem recorded in `path` by the record_untuned option;
+    returns (status, number tuned)."""
+    n = ctypes.c_int(0)
+    st = _lib.mm_tune_file(path.encode(), ctypes.byref(n))
+    return st, n.value
 
 
 def mm_cache_save(path=None):

@@ -194,4 +194,101 @@ mm_status cache_save(DeviceState &ds, const std::string &path) {
   return MM_OK;
 }
 
+namespace {
+std::mutex g_untuned_file_mu;
+
+const char *layout_letters(const Problem &p) {
+  static const char *L[] = {"NN", "NT", "TN", "TT"};
+  return L[(p.at ? 2 : 0) + (p.bt ? 1 : 0)];
+}
+
+bool parse_dtype(const std::string &s, int *t) {
+  if (s == "bf16") *t = MM_BF16;
+  else if (s == "f16") *t = MM_F16;
+  else if (s == "f32") *t = MM_F32;
+  else return false;
+  return true;
+}
+}  // namespace
+
+void record_untuned(DeviceState &ds, const KeyPod &key, const Problem &p, const std::string &path) {
+  {
+    std::lock_guard<std::mutex> lk(ds.untuned_mu);
+    if (!ds.untuned.insert(key).second) return;  // once per key and process
+  }
+  char b[512];
+  snprintf(b, sizeof b, ",%lld,%lld,%lld,%lld,%lld,%lld,%s,%s,%s,%s,%lld,%lld,%lld,%lld\n",
+           (long long)p.M, (long long)p.N, (long long)p.K, (long long)p.lda, (long long)p.ldb,
+           (long long)p.ldc, dtype_name(p.ta), dtype_name(p.tb), dtype_name(p.tc), layout_letters(p),
+           (long long)p.batch, (long long)p.sA, (long long)p.sB, (long long)p.sC);
+  const std::string line = "Untuned," + csv_field(key_text(key)) + b;
+  std::lock_guard<std::mutex> lk(g_untuned_file_mu);
+  FILE *f = fopen(path.c_str(), "a");
+  if (!f) return;  // recording is best effort; the call itself already ran
+  fputs(line.c_str(), f);
+  fclose(f);
+}
+
+mm_status tune_file(DeviceState &ds, const std::string &path, int *tuned) {
+  *tuned = 0;
+  std::ifstream in(path);
+  if (!in) return set_error(MM_ERR_IO, "cannot read %s", path.c_str());
+  const Options o = get_options();
+  sync_table_file(ds, o);
+  std::string line;
+  int lineno = 0;
+  while (std::getline(in, line)) {
+    ++lineno;
+    if (line.empty()) continue;
+    std::vector<std::string> f = csv_split(line);
+    if (f.size() != 16 || f[0] != "Untuned") continue;  // not a record of this format
+    Problem p{};
+    long long v[6], bs[4];
+    for (int i = 0; i < 6; ++i) v[i] = atoll(f[2 + i].c_str());
+    for (int i = 0; i < 4; ++i) bs[i] = atoll(f[12 + i].c_str());
+    if (!parse_dtype(f[8], &p.ta) || !parse_dtype(f[9], &p.tb) || !parse_dtype(f[10], &p.tc) ||
+        f[11].size() != 2)
+      return set_error(MM_ERR_INVALID_ARG, "%s:%d: malformed record", path.c_str(), lineno);
+    p.M = v[0], p.N = v[1], p.K = v[2], p.lda = v[3], p.ldb = v[4], p.ldc = v[5];
+    p.at = f[11][0] == 'T';
+    p.bt = f[11][1] == 'T';
+    p.batch = bs[0], p.sA = bs[1], p.sB = bs[2], p.sC = bs[3];
+    if (p.M < 1 || p.N < 1 || p.K < 1 || p.batch < 1)
+      return set_error(MM_ERR_INVALID_ARG, "%s:%d: empty problem", path.c_str(), lineno);
+    const KeyPod key = make_key(p, o.level);
+    {
+      std::shared_lock<std::shared_mutex> lk(ds.table_mu);
+      if (ds.table.count(key)) continue;  // already tuned
+    }
+    // synthetic operands of the recorded shape (values do not change the
+    // choice: every candidate computes the same product)
+    DevBuf a, bb, c;
+    struct Release {
+      DevBuf &x, &y, &z;
+      ~Release() {
+        x.release();
+        y.release();
+        z.release();
+      }
+    } release{a, bb, c};
+    const size_t na = (size_t)span_a(p) * dtype_bytes(p.ta) + 256;
+    const size_t nb = (size_t)span_b(p) * dtype_bytes(p.tb) + 256;
+    const size_t nc = (size_t)span_c(p) * dtype_bytes(p.tc) + 256;
+    mm_status st;
+    if ((st = a.ensure(na)) != MM_OK || (st = bb.ensure(nb)) != MM_OK || (st = c.ensure(nc)) != MM_OK)
+      return st;
+    MM_CUDA_TRY(cudaMemsetAsync(a.ptr, 0x3c, na, ds.tune_stream));
+    MM_CUDA_TRY(cudaMemsetAsync(bb.ptr, 0x3c, nb, ds.tune_stream));
+    p.A = a.ptr;
+    p.B = bb.ptr;
+    p.C = c.ptr;
+    TableEntry e;
+    st = tune_and_record(ds, p, key, o, nullptr, &e);
+    if (st != MM_OK && st != MM_ERR_PENDING) return st;
+    MM_CUDA_TRY(cudaStreamSynchronize(ds.tune_stream));
+    if (st == MM_OK) ++*tuned;
+  }
+  return MM_OK;
+}
+
 }  // namespace mm

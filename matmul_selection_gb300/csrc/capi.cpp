@@ -124,6 +124,15 @@ mm_status mm_cache_save(const char *path) {
   return cache_save(*ds, f);
 }
 
+mm_status mm_tune_file(const char *path, int *tuned) {
+  if (!path || !tuned) return set_error(MM_ERR_INVALID_ARG, "null path or count");
+  *tuned = 0;
+  DeviceState *ds = nullptr;
+  mm_status st = current_device(&ds);
+  if (st != MM_OK) return st;
+  return tune_file(*ds, path, tuned);
+}
+
 mm_status mm_cache_clear(void) {
   DeviceState *ds = nullptr;
   mm_status st = current_device(&ds);

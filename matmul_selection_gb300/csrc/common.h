@@ -165,6 +165,7 @@ struct Options {
   double peak_tflops = 0.0;
   double peak_gbs = 0.0;
   std::string fault;
+  std::string record_untuned;  // path: keys missed with tuning off are appended here
 };
 // Snapshot of the current options (env values take precedence over the API).
 const Options &get_options();
@@ -222,6 +223,8 @@ struct DeviceState {
   std::mutex pending_mu;
   std::condition_variable pending_cv;
   std::unordered_set<KeyPod, KeyHash, KeyEq> pending;
+  std::mutex untuned_mu;
+  std::unordered_set<KeyPod, KeyHash, KeyEq> untuned;  // keys already recorded this process
   bool file_loaded = false;
   bool dirty = false;
   std::mutex tune_mu;  // one tuning run at a time per device
@@ -326,6 +329,21 @@ mm_status roofline_peaks(DeviceState &ds, Peaks *out);
 
 // ---------------------------------------------------------------- cache file
 mm_status cache_load(DeviceState &ds, const std::string &path);
+// Offline tuning (TunableOp's record-untuned / tune-from-file workflow): a key
+// missed with tuning off is appended once to a file as "Untuned,<key>,<the
+// problem's shape, strides, types and layout>"; tune_file tunes every such
+// problem on library-owned synthetic buffers and records the results.
+void record_untuned(DeviceState &ds, const KeyPod &key, const Problem &p, const std::string &path);
+mm_status tune_file(DeviceState &ds, const std::string &path, int *tuned);
+// The miss path: one tuner per key, then the result into the table.
+// MM_ERR_PENDING (internal): another thread's tuner of the key did not finish
+// within the wait.
+constexpr mm_status MM_ERR_PENDING = 100;
+// order_after: a stream whose pending work tuning must follow (null: none).
+mm_status tune_and_record(DeviceState &ds, const Problem &p, const KeyPod &key, const Options &o,
+                          cudaStream_t order_after, TableEntry *out);
+// The persistent table, loaded once per device before the first tune.
+void sync_table_file(DeviceState &ds, const Options &o);
 mm_status cache_save(DeviceState &ds, const std::string &path);
 std::string device_file_name(const std::string &path, int ordinal);
 

@@ -20,7 +20,8 @@ const OptDef kDefs[] = {{"tuning"},          {"autotune_cache"},
                         {"l2_flush"},        {"numerical_check"},
                         {"cache_file"},      {"decisions"},
                         {"verbose"},         {"peak_tflops"},
-                        {"peak_gbs"},        {"fault"}};
+                        {"peak_gbs"},        {"fault"},
+                        {"record_untuned"}};
 
 std::mutex g_mu;
 Options g_api;
@@ -94,6 +95,7 @@ bool apply(Options &o, const std::string &n, const std::string &v) {
   if (n == "peak_tflops") return parse_double(v, &o.peak_tflops);
   if (n == "peak_gbs") return parse_double(v, &o.peak_gbs);
   if (n == "fault") { o.fault = v; return true; }
+  if (n == "record_untuned") { o.record_untuned = v; return true; }
   return false;
 }
 
@@ -116,6 +118,7 @@ std::string show(const Options &o, const std::string &n) {
   if (n == "peak_tflops") { snprintf(b, sizeof b, "%g", o.peak_tflops); return b; }
   if (n == "peak_gbs") { snprintf(b, sizeof b, "%g", o.peak_gbs); return b; }
   if (n == "fault") return o.fault;
+  if (n == "record_untuned") return o.record_untuned;
   return "";
 }
 

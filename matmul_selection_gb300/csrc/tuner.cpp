@@ -612,6 +612,63 @@ void save_at_exit_fn() {
 
 }  // namespace
 
+void sync_table_file(DeviceState &ds, const Options &o) {
+  if (!o.autotune_cache || o.cache_file.empty() || ds.file_loaded) return;
+  std::unique_lock<std::mutex> tl(ds.tune_mu);
+  if (ds.file_loaded) return;
+  ds.file_loaded = true;
+  cache_load(ds, device_file_name(o.cache_file, ds.info.ordinal));  // absent file: fine
+  static std::once_flag reg_exit;
+  std::call_once(reg_exit, [] { atexit(save_at_exit_fn); });
+}
+
+mm_status tune_and_record(DeviceState &ds, const Problem &p, const KeyPod &key, const Options &o,
+                          cudaStream_t order_after, TableEntry *out) {
+  {  // pending protocol: one tuner per key; others wait (bounded)
+    std::unique_lock<std::mutex> pl(ds.pending_mu);
+    {  // tuned meanwhile by another caller
+      std::shared_lock<std::shared_mutex> lk(ds.table_mu);
+      auto it = ds.table.find(key);
+      if (it != ds.table.end()) {
+        *out = *it->second;
+        return MM_OK;
+      }
+    }
+    if (ds.pending.count(key)) {
+      ds.pending_cv.wait_for(pl, std::chrono::seconds(120), [&] { return !ds.pending.count(key); });
+      pl.unlock();
+      std::shared_lock<std::shared_mutex> lk(ds.table_mu);
+      auto it = ds.table.find(key);
+      if (it != ds.table.end()) {
+        *out = *it->second;
+        return MM_OK;
+      }
+      return MM_ERR_PENDING;
+    }
+    ds.pending.insert(key);
+  }
+  mm_status st;
+  {
+    std::lock_guard<std::mutex> tl(ds.tune_mu);
+    if (order_after) {  // the private stream starts after the caller's pending work
+      cudaEventRecord(ds.ev_order, order_after);
+      cudaStreamWaitEvent(ds.tune_stream, ds.ev_order, 0);
+    }
+    st = tune(ds, p, key, o, out);
+  }
+  {
+    std::lock_guard<std::mutex> pl(ds.pending_mu);
+    if (st == MM_OK) {
+      std::unique_lock<std::shared_mutex> lk(ds.table_mu);
+      ds.table[key] = std::make_shared<const TableEntry>(*out);
+      ds.dirty = true;
+    }
+    ds.pending.erase(key);
+  }
+  ds.pending_cv.notify_all();
+  return st;
+}
+
 mm_status autotune_execute(const Problem &p, cudaStream_t s, ExecResult *res) {
   stats().calls.fetch_add(1, std::memory_order_relaxed);
   if (p.M == 0 || p.N == 0 || p.batch == 0) return MM_OK;
@@ -646,16 +703,13 @@ mm_status autotune_execute(const Problem &p, cudaStream_t s, ExecResult *res) {
     if (res) res->candidate = 0;
     return launch_candidate(0, p, ctx);
   }
-  if (!o.tuning) return launch_default(ds, key, p, ctx, res);
+  if (!o.tuning) {
+    if (!o.record_untuned.empty()) record_untuned(ds, key, p, o.record_untuned);
+    return launch_default(ds, key, p, ctx, res);
+  }
   // sync the persistent table once per device
   if (o.autotune_cache && !o.cache_file.empty() && !ds.file_loaded) {
-    std::unique_lock<std::mutex> tl(ds.tune_mu);
-    if (!ds.file_loaded) {
-      ds.file_loaded = true;
-      cache_load(ds, device_file_name(o.cache_file, ds.info.ordinal));  // absent file: fine
-      static std::once_flag reg_exit;
-      std::call_once(reg_exit, [] { atexit(save_at_exit_fn); });
-    }
+    sync_table_file(ds, o);
     std::shared_lock<std::shared_mutex> lk(ds.table_mu);
     auto it = ds.table.find(key);
     if (it != ds.table.end()) {
@@ -665,41 +719,19 @@ mm_status autotune_execute(const Problem &p, cudaStream_t s, ExecResult *res) {
       return run_entry(ds, *e, p, s, res);
     }
   }
-  // pending protocol: one tuner per key; others wait (bounded)
-  {
-    std::unique_lock<std::mutex> pl(ds.pending_mu);
-    if (ds.pending.count(key)) {
-      ds.pending_cv.wait_for(pl, std::chrono::seconds(120), [&] { return !ds.pending.count(key); });
-      pl.unlock();
-      std::shared_lock<std::shared_mutex> lk(ds.table_mu);
-      auto it = ds.table.find(key);
-      if (it != ds.table.end()) {
-        std::shared_ptr<const TableEntry> e = it->second;
-        lk.unlock();
-        return run_entry(ds, *e, p, s, res);
-      }
-      return launch_default(ds, key, p, ctx, res);
-    }
-    ds.pending.insert(key);
-  }
   TableEntry entry;
-  {
-    std::lock_guard<std::mutex> tl(ds.tune_mu);
-    // the private stream starts after the caller's pending work
-    cudaEventRecord(ds.ev_order, s);
-    cudaStreamWaitEvent(ds.tune_stream, ds.ev_order, 0);
-    st = tune(ds, p, key, o, &entry);
-  }
-  {
-    std::lock_guard<std::mutex> pl(ds.pending_mu);
-    if (st == MM_OK) {
-      std::unique_lock<std::shared_mutex> lk(ds.table_mu);
-      ds.table[key] = std::make_shared<const TableEntry>(entry);
-      ds.dirty = true;
+  st = tune_and_record(ds, p, key, o, s ? s : cudaStreamLegacy, &entry);
+  if (st == MM_ERR_PENDING) {  // another thread's tuner did not finish in time
+    std::shared_lock<std::shared_mutex> lk(ds.table_mu);
+    auto it = ds.table.find(key);
+    if (it != ds.table.end()) {
+      std::shared_ptr<const TableEntry> e = it->second;
+      lk.unlock();
+      return run_entry(ds, *e, p, s, res);
     }
-    ds.pending.erase(key);
+    lk.unlock();
+    return launch_default(ds, key, p, ctx, res);
   }
-  ds.pending_cv.notify_all();
   if (st != MM_OK) return st;
   return run_entry(ds, entry, p, s, res);
 }

@@ -19,7 +19,8 @@ pytestmark = pytest.mark.gpu
 NAMES = mm.candidate_names()
 DEFAULTS = {"tuning": "1", "autotune_cache": "1", "fault": "", "numerical_check": "",
             "decisions": "", "cache_file": "", "max_tuning_iterations": "100",
-            "max_tuning_duration_ms": "30", "l2_flush": "0", "rotating_buffer_mb": "-1"}
+            "max_tuning_duration_ms": "30", "l2_flush": "0", "rotating_buffer_mb": "-1",
+            "record_untuned": ""}
 
 
 @pytest.fixture(autouse=True)
@@ -228,6 +229,37 @@ def test_decision_log(tmp_path):
         assert rec["fastest_index"] == best["index"]
         lead = min(x["median_ms"] for x in measured)
         assert all(x["median_ms"] <= 1.10 * lead + 1e-9 for x in fin)
+
+
+def test_record_untuned_then_tune_file(tmp_path):
+    """Offline tuning: misses with tuning off are recorded once per key;
+    mm_tune_file tunes them on synthetic operands; later calls hit."""
+    path = str(tmp_path / "untuned.csv")
+    mm.check(mm.mm_set_option("tuning", "0"))
+    mm.check(mm.mm_set_option("record_untuned", path))
+    c1 = Case(96, 80, 200, dist="int4").device()
+    c2 = Case(1, 512, 512, layout="NT", dist="int4").device()
+    c3 = Case(12, 40, 72, layout="TN", dt=(BF16, BF16, F32), dist="int4", batch=3,
+              bstride_extra=(8, 16, 8), pad=(8, 8, 4)).device()
+    for c in (c1, c2, c3, c1):  # the repeated key is recorded once
+        mm.check(execute(c))
+        c.check(exact=True)
+    rows = [r for r in open(path).read().splitlines() if r.startswith("Untuned,")]
+    assert len(rows) == 3
+    assert mm.mm_cache_size() == 0 and mm.mm_get_stats()["tunes"] == 0
+    st, n = mm.mm_tune_file(path)
+    assert st == 0 and n == 3, mm.mm_last_error()
+    assert mm.mm_cache_size() == 3
+    before = mm.mm_get_stats()["hits"]
+    for c in (c1, c2, c3):
+        c.device()
+        mm.check(execute(c))
+        c.check(exact=True)
+    assert mm.mm_get_stats()["hits"] == before + 3
+    st, n = mm.mm_tune_file(path)  # nothing left to tune
+    assert st == 0 and n == 0
+    st, n = mm.mm_tune_file(str(tmp_path / "absent.csv"))
+    assert st == mm.MM_ERR_IO
 
 
 def test_finalists_are_retimed(tmp_path):
