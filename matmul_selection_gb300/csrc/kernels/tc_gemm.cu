@@ -824,10 +824,17 @@ __device__ __forceinline__ void pair_unit(const TcParams &p, int u, int bn, int 
     t = p.full_units + (v >> 1);
     half = v & 1;
   }
-  tm = t % p.tiles_m;
-  const int r = t / p.tiles_m;
-  const int tn = r % p.tiles_n;
-  b = r / p.tiles_n;
+  // grouped order: groups of up to 8 row tiles, rows fastest inside a group,
+  // so a wave's A rows and B columns stay within L2 on large problems
+  constexpr int GM = 8;
+  const int per_b = p.tiles_m * p.tiles_n;
+  b = t / per_b;
+  int r = t - b * per_b;
+  const int g = r / (GM * p.tiles_n);
+  const int rows_g = min(GM, p.tiles_m - g * GM);
+  r -= g * GM * p.tiles_n;
+  tm = g * GM + r % rows_g;
+  const int tn = r / rows_g;
   n0 = tn * bn + (half > 0 ? bn / 2 : 0);
   nw = half < 0 ? bn : bn / 2;
 }
