@@ -216,6 +216,23 @@ def run_reference(args, w, name):
 METRIC = "tuned GEMM TFLOP/s & % of roofline at 1 GB300; cold-tune and cache-hit ms"
 
 
+def max_over_ranks(x, world, device):
+    """The largest of a per-rank number over all ranks (the job ends when its
+    slowest replica does); x itself at world 1."""
+    if world <= 1:
+        return x
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_rate(work_per_rank, world, seconds):
+    """Whole-job throughput: every replica does the same work (weak scaling),
+    timed by the slowest rank."""
+    return work_per_rank * world / seconds
+
+
 def ensure_built():
     import importlib.util
     spec = importlib.util.spec_from_file_location(
@@ -366,11 +383,8 @@ def run_ours(args, w, name, rank, world, peaks, quiet=False):
     # every warm step is one call of the tuned candidate: its mean device time
     # per launch is the timed loop's device time over the steps
     kern_ms = total_ms / args.steps
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
-    value = flops * args.steps * world / (total_ms * 1e-3) / 1e12
+    total_ms = max_over_ranks(total_ms, world, dev)
+    value = aggregate_rate(flops * args.steps, world, total_ms * 1e-3) / 1e12
     # context only: the vendor library on the same shape and rotating inputs
     cublas_tflops = None
     if args.cublas and batch == 1 and not w["pad"] and dt[0] == dt[1] and dt[0] != F32:
@@ -406,11 +420,8 @@ def run_ours(args, w, name, rank, world, peaks, quiet=False):
         mm.check(mm.mm_autotune_execute_host(pA.data_ptr(), pB.data_ptr(), pC.data_ptr(), M, N,
                                              K, A.ld, B.ld, C.ld, dt, w["layout"], b, sh))
     e2e_s = time.perf_counter() - t0
-    if world > 1:
-        t = torch.tensor([e2e_s], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_s = float(t.item())
-    e2e_value = flops * e2e_steps * world / e2e_s / 1e12
+    e2e_s = max_over_ranks(e2e_s, world, dev)
+    e2e_value = aggregate_rate(flops * e2e_steps, world, e2e_s) / 1e12
     # roofline of the dominant (tuned) kernel: the bound is whichever of the
     # memory time (algorithmic bytes / HBM peak) and the compute time
     # (flops / tensor peak) is longer
