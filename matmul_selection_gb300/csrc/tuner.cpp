@@ -17,7 +17,7 @@
 //   * the fastest MEDIAN wins; ties go to the lower candidate index;
 //   * unless the round ended inside the limit, the finalists (medians within
 //     10 % of the winner's, at most three) are re-timed in interleaved chunks
-//     and the lowest re-timed median is recorded (the winner's curse: the
+//     of 30 calls and the lowest re-timed median is recorded (the winner's curse: the
 //     fastest of several noisy medians is biased low).
 // Iterations run in chunks (3 for the screening pass, then up to 10), each
 // enqueued behind a short delay kernel so that they run back to back on the
@@ -508,10 +508,12 @@ mm_status tune(DeviceState &ds, const Problem &p, const KeyPod &key, const Optio
       if (fin.size() > 3) fin.resize(3);
       if (fin.size() >= 2) {
         std::vector<std::vector<float>> t(fin.size());
+        // chunks of 30 calls: closer to a long back-to-back run, where a call
+        // overlaps its predecessor's tail (the first call of a chunk cannot)
         for (int round = 0; round < 3; ++round)
           for (size_t f = 0; f < fin.size(); ++f) {
             float ms;
-            if (time_chunk(fin[f], env, round * 10, 10, &ms)) t[f].push_back(ms);
+            if (time_chunk(fin[f], env, round * 30, 30, &ms)) t[f].push_back(ms);
           }
         int pick = -1;
         for (size_t f = 0; f < fin.size(); ++f) {
