@@ -30,7 +30,9 @@
 //   gemv_t_rows  B transposed [N][K].  One warp per output column (row of B)
 //       reading the whole row with 16-byte loads; the dot products end in an
 //       xor-shuffle reduction.  No cross-warp or cross-CTA combination.  The
-//       rows are prefetched into L2 before the wait, as above.
+//       rows are prefetched into L2 before the wait, as above.  A is staged
+//       in shared memory in an order that keeps the lanes' reads of it free
+//       of bank conflicts.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -436,14 +438,38 @@ __global__ void __launch_bounds__(256) gemv_stream_reduce_kernel(const FastArgs 
 }
 
 // ---------------------------------------------------------------- gemv_t_rows
+// A warp walks its row of B in chunks of CE = 32 * VEC elements (512 bytes),
+// lane l holding elements [l * VEC, (l + 1) * VEC) of a chunk.  A sits in
+// shared memory as fp32, one row of KP = (chunks * CE) floats per m, zero past
+// K.  With 16-bit B a lane needs 8 floats of A per chunk; stored in k order
+// they would be 32 bytes apart from lane to lane, and each 16-byte shared load
+// would take two passes.  So each chunk of A is stored as its lanes' first
+// four floats (128 of them), then their last four: element l * 8 + h * 4 + q
+// of a chunk at position h * 128 + l * 4 + q, and a lane's two loads are
+// 16 bytes apart from lane to lane.  With fp32 B (4 floats a lane) k order
+// already has that property.
+template <int VEC>
+__device__ __forceinline__ int trows_k_of_pos(int pos) {
+  if constexpr (VEC == 8) {
+    const int c = pos >> 8, r = pos & 255;
+    const int h = r >> 7, l = (r >> 2) & 31, q = r & 3;
+    return (c << 8) + l * 8 + h * 4 + q;
+  } else {
+    return pos;
+  }
+}
+
 template <int MT, int TB>
 __global__ void __launch_bounds__(kThreads, MT <= 2 ? 2 : 1) gemv_t_rows_kernel(const FastArgs g) {
   pdl_launch_dependents();
   constexpr int EB = TB == MM_F32 ? 4 : 2;
   constexpr int VEC = 16 / EB;
+  constexpr int CE = 32 * VEC;
   constexpr int U = 8;
-  extern __shared__ float fsm[];
-  float *As = fsm;  // [MT][K]
+  extern __shared__ float fsm[];  // dynamic shared memory starts 16-byte aligned
+  float *As = fsm;  // [MT][KP]
+  const int nch = (g.K + CE - 1) / CE;
+  const int KP = nch * CE;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int b = blockIdx.y;
   const int n = blockIdx.x * kWarps + warp;
@@ -459,17 +485,17 @@ __global__ void __launch_bounds__(kThreads, MT <= 2 ? 2 : 1) gemv_t_rows_kernel(
 #pragma unroll
   for (int m = 0; m < MT; ++m) acc[m] = 0.f;
   bool staged = false;
-  for (int kb = 0; kb < g.K; kb += 32 * VEC * U) {
+  for (int c0 = 0; c0 < nch; c0 += U) {
     uint4 v[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      const int k = kb + (u * 32 + lane) * VEC;
-      v[u] = valid ? load16<TB>(row, k, g.K) : make_uint4(0, 0, 0, 0);
+      const int k = (c0 + u) * CE + lane * VEC;
+      v[u] = valid && c0 + u < nch ? load16<TB>(row, k, g.K) : make_uint4(0, 0, 0, 0);
     }
     if (!staged) {
-      stage_batched(g, As, MT * g.K, [&](int e, int64_t *off) {
-        const int m = e / g.K, k = e - m * g.K;
-        if (m >= g.M) return false;
+      stage_batched(g, As, MT * KP, [&](int e, int64_t *off) {
+        const int m = e / KP, k = trows_k_of_pos<VEC>(e - m * KP);
+        if (m >= g.M || k >= g.K) return false;
         *off = (int64_t)b * g.sA + (int64_t)m * g.a_rs + (int64_t)k * g.a_cs;
         return true;
       });
@@ -478,17 +504,26 @@ __global__ void __launch_bounds__(kThreads, MT <= 2 ? 2 : 1) gemv_t_rows_kernel(
     }
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      const int k = kb + (u * 32 + lane) * VEC;
-      if (k < g.K) {
+      const int c = c0 + u;
+      if (c < nch) {  // past K both B (load16) and A (staging) are zero
         float bf[VEC];
         unpack16<TB>(v[u], bf);
 #pragma unroll
         for (int m = 0; m < MT; ++m) {
-          const float *a = As + (int64_t)m * g.K + k;
+          const float *a = As + m * KP + c * CE + lane * 4;
+          const float4 a0 = *reinterpret_cast<const float4 *>(a);
           float t = acc[m];
-#pragma unroll
-          for (int j = 0; j < VEC; ++j)
-            if (k + j < g.K) t = fmaf(a[j], bf[j], t);
+          t = fmaf(a0.x, bf[0], t);
+          t = fmaf(a0.y, bf[1], t);
+          t = fmaf(a0.z, bf[2], t);
+          t = fmaf(a0.w, bf[3], t);
+          if constexpr (VEC == 8) {
+            const float4 a1 = *reinterpret_cast<const float4 *>(a + 128);
+            t = fmaf(a1.x, bf[4], t);
+            t = fmaf(a1.y, bf[5], t);
+            t = fmaf(a1.z, bf[6], t);
+            t = fmaf(a1.w, bf[7], t);
+          }
           acc[m] = t;
         }
       }
@@ -539,7 +574,9 @@ constexpr size_t kMaxSmem = 96 * 1024;
 size_t smem_n(int mt, int ks, int eb) {
   return ((size_t)ks * mt + (size_t)kWarps * mt * (256 / eb)) * sizeof(float);
 }
-size_t smem_t(int mt, int64_t K) { return (size_t)mt * K * sizeof(float); }
+// gemv_t_rows: A as fp32 rows padded to whole 512-byte chunks of B (at most
+// 256 elements a chunk).
+size_t smem_t(int mt, int64_t K) { return (size_t)mt * ((K + 255) / 256 * 256) * sizeof(float); }
 size_t smem_stream(int mt, int ks, int eb) {
   return ((size_t)ks * mt + (size_t)kStreamWarps * mt * (256 / eb)) * sizeof(float);
 }

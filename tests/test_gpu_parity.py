@@ -157,13 +157,13 @@ def test_results_deterministic():
 @pytest.mark.parametrize("dt", [(BF16, BF16, F32), (F16, F16, F16), (F32, F32, F32)],
                          ids=["bf16-f32", "f16-f16", "f32-f32"])
 def test_gemv_n_stream_splits(shape, dt):
-    """The split-K GEMV with a ticketed last-block sum: single and many K
-    splits, a ragged last column group, and three launches in a row (the
-    tickets must re-arm)."""
+    """The split-K GEMV whose split sums a second kernel adds: single and
+    many K splits, a ragged last column group, and three launches in a row
+    over a fresh output each time."""
     i = NAMES.index("gemv_n_stream")
     c = Case(*shape, layout="NN", dt=dt, dist="int4", seed=sum(shape)).device()
     for _ in range(3):
-        c.device()  # a fresh output each time: a ticket left armed would leave it unwritten
+        c.device()  # a fresh output each time: a launch that skipped a column would show
         assert run(i, c) == mm.MM_OK, mm.mm_last_error()
         c.check(exact=True)
     # batched with gaps; B rows of 304 elements keep the 16-byte row alignment
@@ -171,6 +171,19 @@ def test_gemv_n_stream_splits(shape, dt):
               pad=(8, 8, 4)).device()
     assert run(i, cb) == mm.MM_OK, mm.mm_last_error()
     cb.check(exact=True)
+
+
+@pytest.mark.parametrize("shape", [(1, 4096, 4096), (3, 37, 4104), (8, 64, 2056), (2, 20, 104),
+                                   (1, 17, 8)], ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("dt", [(BF16, BF16, BF16), (F32, F32, F32)], ids=["bf16", "f32"])
+def test_gemv_t_rows_chunks(shape, dt):
+    """The row-per-warp GEMV walks each row in 512-byte chunks from a
+    starting chunk of its own, wrapping at the row's end: whole and ragged
+    last chunks, rows shorter than one chunk, and a partial last CTA."""
+    i = NAMES.index("gemv_t_rows")
+    c = Case(*shape, layout="NT", dt=dt, dist="int4", seed=sum(shape)).device()
+    assert run(i, c) == mm.MM_OK, mm.mm_last_error()
+    c.check(exact=True)
 
 
 # ---------------------------------------------------------------- full sizes
