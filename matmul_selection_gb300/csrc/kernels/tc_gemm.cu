@@ -22,8 +22,9 @@
 //     multiplied as tf32: the burn backend page notes the kernel may run f32
 //     as tf32), fp32 accumulation always;
 //   * split-K configurations write fp32 partials of each K slice to a
-//     workspace; a second kernel adds the slices in increasing slice order
-//     (deterministic) and converts.  Split-K regroups additions only (the
+//     workspace; a second kernel adds the slices in a fixed order (runs of
+//     consecutive slices, each in increasing order, then the runs in order;
+//     deterministic) and converts.  Split-K regroups additions only (the
 //     CMU 15-779 lecture's rfactor / split-K discussion);
 //   * every mbarrier wait is bounded (%globaltimer); on expiry the kernel
 //     records an error code, tells the other roles to stop, waits for its own
@@ -1075,28 +1076,63 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (warp == 1) tmem_dealloc_pair(tmem_base, TMEM_COLS);
 }
 
-// Sum the split-K partials in increasing slice order and convert.
-__global__ void splitk_reduce_kernel(const float *__restrict__ ws, int S, int batch, int M, int N,
-                                     void *C, int tc, int64_t ldc, int64_t sC, int c_trans) {
+// Sum the split-K partials in a fixed order and convert.  G threads (a power
+// of two dividing the block) share an output element: thread g adds the
+// slices of run g, [g * run, (g + 1) * run) with run = ceil(S / G), in
+// increasing order, and the G run sums are then added in run order.  G comes
+// from the problem shape and the SM count only, so every launch of a problem
+// adds the same numbers in the same order; G = 1 is the plain s = 0..S-1 sum.
+// Loads are issued eight at a time so their latencies overlap.  RUNS = false
+// is the G = 1 instance: no shared memory and no block barrier, so its blocks
+// fit beside a GEMM CTA that holds nearly all of an SM's shared memory, are
+// resident early, and start the moment the GEMM's partials are complete.
+template <bool RUNS>
+__global__ void __launch_bounds__(256) splitk_reduce_kernel(const float *__restrict__ ws, int S,
+                                                            int G, int batch, int M, int N, void *C,
+                                                            int tc, int64_t ldc, int64_t sC,
+                                                            int c_trans) {
   pdl_launch_dependents();
   pdl_wait();
+  extern __shared__ float runs[];  // [256], RUNS only
+  if (!RUNS) G = 1;
+  const int per = 256 / G;  // elements a block handles per pass
+  const int g = threadIdx.x / per, el = threadIdx.x - g * per;
+  const int run = (S + G - 1) / G;
+  const int q0 = g * run, q1 = min(S, q0 + run);
   const int64_t total = (int64_t)batch * M * N;  // flattened [batch][M][N]
   const bool narrow = total < (1LL << 32);       // 32-bit index arithmetic suffices
-  for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total;
-       e += (int64_t)gridDim.x * blockDim.x) {
+  for (int64_t base = (int64_t)blockIdx.x * per; base < total; base += (int64_t)gridDim.x * per) {
+    const int64_t e = base + el;
     float sum = 0.f;
-    for (int q = 0; q < S; ++q) sum += __ldcs(ws + q * total + e);
-    int64_t rg, j;  // row of [batch][M], column
-    if (narrow) {
-      const uint32_t r32 = (uint32_t)e / (uint32_t)N;
-      rg = r32;
-      j = (uint32_t)e - r32 * (uint32_t)N;
-    } else {
-      rg = e / N;
-      j = e - rg * N;
+    if (e < total)
+      for (int q = q0; q < q1; q += 8) {
+        float v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) v[u] = q + u < q1 ? __ldcs(ws + (int64_t)(q + u) * total + e) : 0.f;
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          if (q + u < q1) sum += v[u];
+      }
+    if constexpr (RUNS) {
+      runs[threadIdx.x] = sum;
+      __syncthreads();
+      if (g == 0)
+        for (int r = 1; r < G; ++r) sum += runs[r * per + el];
     }
-    const int64_t b = batch == 1 ? 0 : rg / M, i = rg - b * M;
-    store_one(C, tc, c_trans ? b * sC + j * ldc + i : b * sC + i * ldc + j, sum);
+    if (g == 0 && e < total) {
+      int64_t rg, j;  // row of [batch][M], column
+      if (narrow) {
+        const uint32_t r32 = (uint32_t)e / (uint32_t)N;
+        rg = r32;
+        j = (uint32_t)e - r32 * (uint32_t)N;
+      } else {
+        rg = e / N;
+        j = e - rg * N;
+      }
+      const int64_t b = batch == 1 ? 0 : rg / M, i = rg - b * M;
+      store_one(C, tc, c_trans ? b * sC + j * ldc + i : b * sC + i * ldc + j, sum);
+    }
+    if constexpr (RUNS) __syncthreads();
   }
 }
 
@@ -1299,11 +1335,32 @@ mm_status dispatch(int cfg, const CUtensorMap &ma, const CUtensorMap &mb, const 
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
-// Grid of the split-K reduction: one element a thread, about eight blocks of
-// 256 threads an SM.
-dim3 reduce_grid(const TcParams &tp, int sms) {
+// Split-K reduction plan: G threads an element (a power of two <= 32), grown
+// while a thread's run is longer than 8 slices and the GPU still holds the
+// threads (the run's loads then take one or two trips to L2 instead of S / 8);
+// about eight blocks of 256 threads an SM.
+struct ReducePlan {
+  dim3 grid;
+  int G;
+};
+ReducePlan reduce_plan(const TcParams &tp, int sms) {
   const int64_t total = (int64_t)tp.batch * tp.M * tp.N;
-  return dim3((unsigned)std::max<int64_t>(1, std::min<int64_t>(ceil_div(total, 256), (int64_t)sms * 8)));
+  int G = 1;
+  while (G < 32 && ceil_div(tp.splits, G) > 8 && total * G * 2 <= (int64_t)sms * 2048) G *= 2;
+  const int64_t per = 256 / G;
+  const int64_t blocks = std::max<int64_t>(1, std::min<int64_t>(ceil_div(total, per), (int64_t)sms * 8));
+  return {dim3((unsigned)blocks), G};
+}
+
+mm_status launch_reduce(const TcParams &tp, int sms, const Problem &p, int c_trans, cudaStream_t s) {
+  const ReducePlan rp = reduce_plan(tp, sms);
+  cudaError_t e =
+      rp.G > 1 ? launch_pdl(splitk_reduce_kernel<true>, rp.grid, dim3(256), 256 * sizeof(float), s,
+                            dim3(1), tp.ws, tp.splits, rp.G, tp.batch, tp.M, tp.N, p.C, p.tc, p.ldc,
+                            p.sC, c_trans)
+               : launch_pdl(splitk_reduce_kernel<false>, rp.grid, dim3(256), 0, s, dim3(1), tp.ws,
+                            tp.splits, 1, tp.batch, tp.M, tp.N, p.C, p.tc, p.ldc, p.sC, c_trans);
+  return e == cudaSuccess ? MM_OK : cuda_error(e, "splitk_reduce_kernel launch");
 }
 
 // Split count for a split-K configuration: enough units to fill the SMs.
@@ -1397,10 +1454,7 @@ mm_status launch_tc_splitk_into(const Problem &p, const DeviceInfo &di, int cfg,
   const int grid = (int)std::min<int64_t>(units, di.sms);
   st = es == 2 ? dispatch<2>(cfg, ma, mb, ma, tp, grid, s) : dispatch<4>(cfg, ma, mb, ma, tp, grid, s);
   if (st != MM_OK) return st;
-  cudaError_t e = launch_pdl(splitk_reduce_kernel, reduce_grid(tp, di.sms), dim3(256), 0, s, dim3(1),
-                             tp.ws, tp.splits, tp.batch, tp.M, tp.N, p.C, p.tc, p.ldc, p.sC, 0);
-  if (e != cudaSuccess) return cuda_error(e, "splitk_reduce_kernel launch");
-  return MM_OK;
+  return launch_reduce(tp, di.sms, p, 0, s);
 }
 
 int tc_config_index(const char *name) {
@@ -1619,13 +1673,7 @@ mm_status launch_tc_impl(const Problem &p, LaunchCtx &ctx, int cfg, bool c_trans
   st = es == 2 ? dispatch<2>(cfg, ma, mb, mc, tp, grid, ctx.stream)
                : dispatch<4>(cfg, ma, mb, mc, tp, grid, ctx.stream);
   if (st != MM_OK) return st;
-  if (tp.splits > 1) {
-    cudaError_t e = launch_pdl(splitk_reduce_kernel, reduce_grid(tp, ctx.dev->info.sms), dim3(256), 0,
-                               ctx.stream, dim3(1),
-                               tp.ws, tp.splits, tp.batch, tp.M, tp.N, p.C, p.tc, p.ldc, p.sC,
-                               tp.c_trans);
-    if (e != cudaSuccess) return cuda_error(e, "splitk_reduce_kernel launch");
-  }
+  if (tp.splits > 1) return launch_reduce(tp, ctx.dev->info.sms, p, tp.c_trans, ctx.stream);
   return MM_OK;
 }
 

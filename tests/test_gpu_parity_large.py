@@ -70,3 +70,44 @@ def test_tuned_square_real_valued_sampled():
     got = oracle.decode(flat[pts[:, 1] * c.C.ld + pts[:, 2]], BF16)
     err = np.linalg.norm(got - ref) / np.linalg.norm(ref)
     assert err <= 2e-3, err
+
+
+SPLITK = [i for i, n in enumerate(NAMES) if "splitk" in n]
+
+
+@pytest.fixture(scope="module")
+def splitk_case():
+    c = Case(128, 128, 65536, layout="NN", dt=(BF16, BF16, F32), dist="int4", seed=43)
+    c.device()
+    return c
+
+
+@pytest.mark.parametrize("cand", SPLITK, ids=[NAMES[i] for i in SPLITK])
+def test_splitk_full_size_exact(splitk_case, cand):
+    """The split-K workload at full size (128 x 128 x 65536): dozens of K
+    slices a tile, so several threads share each output in the reduction.
+    Entries in {-4..4} keep every partial sum below 2^24 in magnitude, exact
+    in fp32 in any order."""
+    c = splitk_case
+    c.dC.fill_(0xFF)
+    st = mm.mm_execute_candidate(cand, *c.args())
+    if st == mm.MM_ERR_UNSUPPORTED:
+        pytest.skip(mm.mm_last_error())
+    assert st == 0, mm.mm_last_error()
+    c.check(exact=True)
+
+
+@pytest.mark.parametrize("cand", SPLITK, ids=[NAMES[i] for i in SPLITK])
+def test_splitk_full_size_real_repeatable(cand):
+    """Real-valued inputs at the same size: within the Frobenius bound, and
+    two launches give the same bytes (the slice sums are added in a fixed
+    order)."""
+    c = Case(128, 128, 65536, layout="NN", dt=(BF16, BF16, BF16), dist="normal", seed=44).device()
+    st = mm.mm_execute_candidate(cand, *c.args())
+    if st == mm.MM_ERR_UNSUPPORTED:
+        pytest.skip(mm.mm_last_error())
+    assert st == 0, mm.mm_last_error()
+    c.check(exact=False)
+    first = c.result().copy()
+    assert mm.mm_execute_candidate(cand, *c.args()) == 0
+    assert np.array_equal(first.view(np.uint8), c.result().view(np.uint8))
