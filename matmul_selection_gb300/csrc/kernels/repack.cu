@@ -11,6 +11,7 @@
 // of the product's time, against the naive kernel otherwise left.  The swap
 // variant (GEMV group) serves small M: it copies the few rows of A and runs
 // the split-K configuration on C^T = B^T A^T.
+#include <algorithm>
 #include <type_traits>
 
 #include "../common.h"
@@ -20,11 +21,16 @@ namespace mm {
 namespace {
 
 // Copy `rows` rows of `row_bytes` from a strided source to a strided
-// destination, G bytes per thread step (G divides every address and size).
+// destination, G bytes a piece (G divides every address and size).  Grid y
+// walks the rows of all batch items (one division a row), grid x a row's
+// pieces; each thread issues its U loads before its U stores.
+constexpr int kRepackU = 4;
 template <int G>
-__global__ void repack_kernel(const char *__restrict__ src, char *__restrict__ dst, int64_t rows,
-                              int64_t row_bytes, int64_t src_ld, int64_t dst_ld, int64_t batch,
-                              int64_t src_bs, int64_t dst_bs) {
+__global__ void __launch_bounds__(256) repack_kernel(const char *__restrict__ src,
+                                                     char *__restrict__ dst, int64_t rows,
+                                                     int64_t row_bytes, int64_t src_ld,
+                                                     int64_t dst_ld, int64_t batch, int64_t src_bs,
+                                                     int64_t dst_bs) {
   pdl_launch_dependents();
   pdl_wait();
   using T = typename std::conditional<
@@ -32,12 +38,25 @@ __global__ void repack_kernel(const char *__restrict__ src, char *__restrict__ d
       typename std::conditional<G == 8, uint2,
                                 typename std::conditional<G == 4, uint32_t, uint16_t>::type>::type>::type;
   const int64_t units = row_bytes / G;
-  const int64_t total = batch * rows * units;
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
-       i += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t u = i % units, r = (i / units) % rows, b = i / (units * rows);
-    const T v = *reinterpret_cast<const T *>(src + b * src_bs + r * src_ld + u * G);
-    *reinterpret_cast<T *>(dst + b * dst_bs + r * dst_ld + u * G) = v;
+  const int64_t nrows = batch * rows;
+  for (int64_t rr = blockIdx.y; rr < nrows; rr += gridDim.y) {
+    const int64_t b = rr / rows, r = rr - b * rows;
+    const char *s = src + b * src_bs + r * src_ld;
+    char *d = dst + b * dst_bs + r * dst_ld;
+    for (int64_t u0 = (int64_t)blockIdx.x * (256 * kRepackU) + threadIdx.x; u0 < units;
+         u0 += (int64_t)gridDim.x * (256 * kRepackU)) {
+      T v[kRepackU];
+#pragma unroll
+      for (int k = 0; k < kRepackU; ++k) {
+        const int64_t u = u0 + k * 256;
+        if (u < units) v[k] = *reinterpret_cast<const T *>(s + u * G);
+      }
+#pragma unroll
+      for (int k = 0; k < kRepackU; ++k) {
+        const int64_t u = u0 + k * 256;
+        if (u < units) *reinterpret_cast<T *>(d + u * G) = v[k];
+      }
+    }
   }
 }
 
@@ -110,17 +129,21 @@ mm_status repack(const void *src, void *dst, int64_t rows, int64_t row_bytes, in
     return (uintptr_t)src % g == 0 && (uintptr_t)dst % g == 0 && row_bytes % g == 0 &&
            src_ld % g == 0 && dst_ld % g == 0 && (batch <= 1 || (src_bs % g == 0 && dst_bs % g == 0));
   };
-  const int64_t total_bytes = batch * rows * row_bytes;
   int g = ok(16) ? 16 : ok(8) ? 8 : ok(4) ? 4 : 2;
-  int64_t units = total_bytes / g;
-  int blocks = (int)std::min<int64_t>((units + 255) / 256, (int64_t)sms * 16);
-  if (blocks < 1) blocks = 1;
+  // x: enough blocks to cover a row, y: the rows (capped; the kernel strides),
+  // about 16 blocks an SM in all
+  const int64_t nrows = std::max<int64_t>(1, batch * rows);
+  const int64_t per_block = 256LL * kRepackU;
+  const int64_t cap = (int64_t)sms * 16;
+  int64_t gx = std::max<int64_t>(1, (row_bytes / g + per_block - 1) / per_block);
+  gx = std::min<int64_t>(gx, cap);
+  const int64_t gy = std::min<int64_t>({nrows, 65535, std::max<int64_t>(1, cap / gx)});
   const char *sp = static_cast<const char *>(src);
   char *dp = static_cast<char *>(dst);
   auto kern = g == 16 ? repack_kernel<16> : g == 8 ? repack_kernel<8> : g == 4 ? repack_kernel<4>
                                                                            : repack_kernel<2>;
-  cudaError_t e = launch_pdl(kern, dim3(blocks), dim3(256), 0, s, dim3(1), sp, dp, rows, row_bytes,
-                             src_ld, dst_ld, batch, src_bs, dst_bs);
+  cudaError_t e = launch_pdl(kern, dim3((unsigned)gx, (unsigned)gy), dim3(256), 0, s, dim3(1), sp,
+                             dp, rows, row_bytes, src_ld, dst_ld, batch, src_bs, dst_bs);
   return e == cudaSuccess ? MM_OK : cuda_error(e, "repack_kernel launch");
 }
 

@@ -75,7 +75,9 @@ struct TcParams {
   // output stored transposed: element (i, j) of the computed product goes to
   // C[j * ldc + i] (the swapped form C^T = B^T A^T of a product with small M)
   int c_trans;
-  int c_tma;  // 1-SM kernel: C written by TMA bulk-tensor stores (tmC valid)
+  // 1-SM kernel: C written by TMA bulk-tensor stores (tmC valid); with
+  // splits > 1, tmC maps the fp32 workspace as [splits * batch][M][N]
+  int c_tma;
   uint64_t timeout_ns;
   // 2-SM kernel: units [0, full_units) are whole tiles; the remaining tiles
   // of the last partial wave are split along N into two half-width units
@@ -609,11 +611,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
       const bool rows_full = row0 + 32 <= p.M && !p.c_trans;
       if (p.c_tma) {
-        // 128-byte rows: 32 f32 or 64 16-bit columns per box; lane = row of the box
-        const bool f32 = p.tc == MM_F32, bf = p.tc == MM_BF16;
+        // 128-byte rows: 32 f32 or 64 16-bit columns per box; lane = row of the box.
+        // Split-K partials are f32 boxes of the workspace map, item sp * batch + b.
+        const bool f32 = p.splits > 1 || p.tc == MM_F32, bf = p.tc == MM_BF16;
+        const int zc = p.splits > 1 ? sp * p.batch + b : b;
         const int cols = f32 ? 32 : 64;
+        // Only boxes that start inside C are staged, and each staged box is
+        // stored: the wait below counts on every box written since the other
+        // buffer's store having committed its own store (a skipped store would
+        // let this box be refilled while its store still reads it).
+        const int cend = row0 < p.M ? min(BN, p.N - tn * BN) : 0;
 #pragma unroll 1
-        for (int c = 0; c < BN; c += cols) {
+        for (int c = 0; c < cend; c += cols) {
           uint32_t r0[32], r1[32];
           tmem_ld_32cols(tbase + (uint32_t)c, r0);
           if (!f32) tmem_ld_32cols(tbase + (uint32_t)(c + 32), r1);
@@ -641,8 +650,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
           fence_proxy_async_smem();
           __syncwarp();
-          if (lane == 0 && tn * BN + c < p.N && row0 < p.M)  // partial boxes are clipped
-            tma_store_3d(&tmC, smem_u32(box), tn * BN + c, row0, b);
+          if (lane == 0)  // rows and columns past C are clipped by the copy
+            tma_store_3d(&tmC, smem_u32(box), tn * BN + c, row0, zc);
           sbuf ^= 1;
         }
       } else
@@ -1077,60 +1086,105 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 }
 
 // Sum the split-K partials in a fixed order and convert.  G threads (a power
-// of two dividing the block) share an output element: thread g adds the
-// slices of run g, [g * run, (g + 1) * run) with run = ceil(S / G), in
-// increasing order, and the G run sums are then added in run order.  G comes
-// from the problem shape and the SM count only, so every launch of a problem
-// adds the same numbers in the same order; G = 1 is the plain s = 0..S-1 sum.
-// Loads are issued eight at a time so their latencies overlap.  RUNS = false
-// is the G = 1 instance: no shared memory and no block barrier, so its blocks
-// fit beside a GEMM CTA that holds nearly all of an SM's shared memory, are
-// resident early, and start the moment the GEMM's partials are complete.
-template <bool RUNS>
+// of two dividing the block) share a group of V consecutive outputs of the
+// flattened [batch][M][N] grid: thread g adds the slices of run g,
+// [g * run, (g + 1) * run) with run = ceil(S / G), in increasing order, and
+// the G run sums are then added in run order.  G comes from the problem shape
+// and the SM count only, so every launch of a problem adds the same numbers in
+// the same order; G = 1 is the plain s = 0..S-1 sum.  With V = 4 a slice's
+// four outputs come in one 16-byte load (the workspace is 16-byte aligned and
+// a slice holds a multiple of four floats).  Loads are issued eight at a time
+// so their latencies overlap.  RUNS = false is the G = 1 instance: no shared
+// memory and no block barrier, so its blocks fit beside a GEMM CTA that holds
+// nearly all of an SM's shared memory, are resident early, and start the
+// moment the GEMM's partials are complete.
+template <bool RUNS, int V>
 __global__ void __launch_bounds__(256) splitk_reduce_kernel(const float *__restrict__ ws, int S,
                                                             int G, int batch, int M, int N, void *C,
                                                             int tc, int64_t ldc, int64_t sC,
                                                             int c_trans) {
   pdl_launch_dependents();
   pdl_wait();
-  extern __shared__ float runs[];  // [256], RUNS only
+  extern __shared__ float runs[];  // [V][256], RUNS only
   if (!RUNS) G = 1;
-  const int per = 256 / G;  // elements a block handles per pass
+  const int per = 256 / G;  // output groups a block handles per pass
   const int g = threadIdx.x / per, el = threadIdx.x - g * per;
   const int run = (S + G - 1) / G;
   const int q0 = g * run, q1 = min(S, q0 + run);
   const int64_t total = (int64_t)batch * M * N;  // flattened [batch][M][N]
+  const int64_t groups = (total + V - 1) / V;
   const bool narrow = total < (1LL << 32);       // 32-bit index arithmetic suffices
-  for (int64_t base = (int64_t)blockIdx.x * per; base < total; base += (int64_t)gridDim.x * per) {
-    const int64_t e = base + el;
-    float sum = 0.f;
-    if (e < total)
-      for (int q = q0; q < q1; q += 8) {
-        float v[8];
+  for (int64_t base = (int64_t)blockIdx.x * per; base < groups; base += (int64_t)gridDim.x * per) {
+    const int64_t e0 = (base + el) * V;
+    float sum[V];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) v[u] = q + u < q1 ? __ldcs(ws + (int64_t)(q + u) * total + e) : 0.f;
+    for (int k = 0; k < V; ++k) sum[k] = 0.f;
+    if (e0 < total) {
+      const float *pq = ws + (int64_t)q0 * total + e0;
+      if (V == 4 && e0 + 4 <= total) {
+        for (int q = q0; q < q1; q += 8) {
+          float4 v[8];
 #pragma unroll
-        for (int u = 0; u < 8; ++u)
-          if (q + u < q1) sum += v[u];
+          for (int u = 0; u < 8; ++u) {
+            v[u] = q + u < q1 ? __ldcs(reinterpret_cast<const float4 *>(pq)) : make_float4(0, 0, 0, 0);
+            pq += total;
+          }
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            if (q + u < q1) {
+              sum[0] += v[u].x;
+              sum[1 % V] += v[u].y;
+              sum[2 % V] += v[u].z;
+              sum[3 % V] += v[u].w;
+            }
+        }
+      } else {
+        for (int q = q0; q < q1; q += 8) {
+          float v[8][V];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+#pragma unroll
+            for (int k = 0; k < V; ++k) v[u][k] = q + u < q1 && e0 + k < total ? __ldcs(pq + k) : 0.f;
+            pq += total;
+          }
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            if (q + u < q1)
+#pragma unroll
+              for (int k = 0; k < V; ++k) sum[k] += v[u][k];
+        }
       }
+    }
     if constexpr (RUNS) {
-      runs[threadIdx.x] = sum;
+#pragma unroll
+      for (int k = 0; k < V; ++k) runs[k * 256 + threadIdx.x] = sum[k];
       __syncthreads();
       if (g == 0)
-        for (int r = 1; r < G; ++r) sum += runs[r * per + el];
+        for (int r = 1; r < G; ++r)
+#pragma unroll
+          for (int k = 0; k < V; ++k) sum[k] += runs[k * 256 + r * per + el];
     }
-    if (g == 0 && e < total) {
-      int64_t rg, j;  // row of [batch][M], column
+    if (g == 0 && e0 < total) {
+      int64_t rg, j;  // row of [batch][M], column of the group's first output
       if (narrow) {
-        const uint32_t r32 = (uint32_t)e / (uint32_t)N;
+        const uint32_t r32 = (uint32_t)e0 / (uint32_t)N;
         rg = r32;
-        j = (uint32_t)e - r32 * (uint32_t)N;
+        j = (uint32_t)e0 - r32 * (uint32_t)N;
       } else {
-        rg = e / N;
-        j = e - rg * N;
+        rg = e0 / N;
+        j = e0 - rg * N;
       }
-      const int64_t b = batch == 1 ? 0 : rg / M, i = rg - b * M;
-      store_one(C, tc, c_trans ? b * sC + j * ldc + i : b * sC + i * ldc + j, sum);
+#pragma unroll
+      for (int k = 0; k < V; ++k) {
+        if (e0 + k < total) {
+          const int64_t b = batch == 1 ? 0 : rg / M, i = rg - b * M;
+          store_one(C, tc, c_trans ? b * sC + j * ldc + i : b * sC + i * ldc + j, sum[k]);
+        }
+        if (++j == N) {
+          j = 0;
+          ++rg;
+        }
+      }
     }
     if constexpr (RUNS) __syncthreads();
   }
@@ -1335,31 +1389,55 @@ mm_status dispatch(int cfg, const CUtensorMap &ma, const CUtensorMap &mb, const 
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
-// Split-K reduction plan: G threads an element (a power of two <= 32), grown
-// while a thread's run is longer than 8 slices and the GPU still holds the
-// threads (the run's loads then take one or two trips to L2 instead of S / 8);
-// about eight blocks of 256 threads an SM.
+// Split-K reduction plan: V = 4 outputs a thread when the workspace allows
+// 16-byte loads, else 1; G threads a group of V outputs (a power of two
+// <= 32), grown while a thread's run is longer than 8 slices and the GPU
+// still holds the threads (the run's loads then take one or two trips to L2
+// instead of S / 8); about eight blocks of 256 threads an SM.
 struct ReducePlan {
   dim3 grid;
-  int G;
+  int G, V;
 };
 ReducePlan reduce_plan(const TcParams &tp, int sms) {
   const int64_t total = (int64_t)tp.batch * tp.M * tp.N;
+  const int V = (uintptr_t)tp.ws % 16 == 0 && total % 4 == 0 ? 4 : 1;
+  const int64_t groups = ceil_div(total, V);
   int G = 1;
-  while (G < 32 && ceil_div(tp.splits, G) > 8 && total * G * 2 <= (int64_t)sms * 2048) G *= 2;
+  while (G < 32 && ceil_div(tp.splits, G) > 8 && groups * G * 2 <= (int64_t)sms * 2048) G *= 2;
   const int64_t per = 256 / G;
-  const int64_t blocks = std::max<int64_t>(1, std::min<int64_t>(ceil_div(total, per), (int64_t)sms * 8));
-  return {dim3((unsigned)blocks), G};
+  const int64_t blocks = std::max<int64_t>(1, std::min<int64_t>(ceil_div(groups, per), (int64_t)sms * 8));
+  return {dim3((unsigned)blocks), G, V};
+}
+
+// The split-K workspace [splits * batch][M][N] (fp32) as the target of the
+// epilogue's bulk-tensor stores, 32 x 32 boxes.  Needs 16-byte aligned rows;
+// leaves tp.c_tma at 0 (per-thread stores) otherwise.
+mm_status ws_map(CUtensorMap *map, TcParams &tp) {
+  const uint64_t row = (uint64_t)tp.N * 4, item = row * (uint64_t)tp.M;
+  if ((uintptr_t)tp.ws % 16 || row % 16 || item >= (1ULL << 40)) return MM_OK;
+  mm_status st = encode_map(map, MM_F32, tp.ws, tp.N, tp.M, (uint64_t)tp.splits * tp.batch, row,
+                            item, 32, 32);
+  if (st == MM_OK) tp.c_tma = 1;
+  return st;
+}
+
+template <bool RUNS, int V>
+cudaError_t launch_reduce_t(const ReducePlan &rp, const TcParams &tp, const Problem &p, int c_trans,
+                            cudaStream_t s) {
+  const size_t smem = RUNS ? (size_t)V * 256 * sizeof(float) : 0;
+  return launch_pdl(splitk_reduce_kernel<RUNS, V>, rp.grid, dim3(256), smem, s, dim3(1), tp.ws,
+                    tp.splits, rp.G, tp.batch, tp.M, tp.N, p.C, p.tc, p.ldc, p.sC, c_trans);
 }
 
 mm_status launch_reduce(const TcParams &tp, int sms, const Problem &p, int c_trans, cudaStream_t s) {
   const ReducePlan rp = reduce_plan(tp, sms);
-  cudaError_t e =
-      rp.G > 1 ? launch_pdl(splitk_reduce_kernel<true>, rp.grid, dim3(256), 256 * sizeof(float), s,
-                            dim3(1), tp.ws, tp.splits, rp.G, tp.batch, tp.M, tp.N, p.C, p.tc, p.ldc,
-                            p.sC, c_trans)
-               : launch_pdl(splitk_reduce_kernel<false>, rp.grid, dim3(256), 0, s, dim3(1), tp.ws,
-                            tp.splits, 1, tp.batch, tp.M, tp.N, p.C, p.tc, p.ldc, p.sC, c_trans);
+  cudaError_t e;
+  if (rp.G > 1)
+    e = rp.V == 4 ? launch_reduce_t<true, 4>(rp, tp, p, c_trans, s)
+                  : launch_reduce_t<true, 1>(rp, tp, p, c_trans, s);
+  else
+    e = rp.V == 4 ? launch_reduce_t<false, 4>(rp, tp, p, c_trans, s)
+                  : launch_reduce_t<false, 1>(rp, tp, p, c_trans, s);
   return e == cudaSuccess ? MM_OK : cuda_error(e, "splitk_reduce_kernel launch");
 }
 
@@ -1452,7 +1530,10 @@ mm_status launch_tc_splitk_into(const Problem &p, const DeviceInfo &di, int cfg,
   tp.b_box_stride = mn_atom_bytes;
   tp.ws = ws;
   const int grid = (int)std::min<int64_t>(units, di.sms);
-  st = es == 2 ? dispatch<2>(cfg, ma, mb, ma, tp, grid, s) : dispatch<4>(cfg, ma, mb, ma, tp, grid, s);
+  CUtensorMap mw = ma;
+  st = ws_map(&mw, tp);
+  if (st != MM_OK) return st;
+  st = es == 2 ? dispatch<2>(cfg, ma, mb, mw, tp, grid, s) : dispatch<4>(cfg, ma, mb, mw, tp, grid, s);
   if (st != MM_OK) return st;
   return launch_reduce(tp, di.sms, p, 0, s);
 }
@@ -1661,11 +1742,15 @@ mm_status launch_tc_impl(const Problem &p, LaunchCtx &ctx, int cfg, bool c_trans
     tp.ws = static_cast<float *>(w);
   }
   const int grid = (int)std::min<int64_t>(units, ctx.dev->info.sms);
-  // C by bulk-tensor stores where TMA can describe it (else the per-thread path)
+  // C (or the split-K workspace) by bulk-tensor stores where TMA can describe
+  // it, else the per-thread path
   CUtensorMap mc = ma;
-  if (!c_trans && tp.splits == 1 && (uintptr_t)p.C % 16 == 0 && (p.ldc * ec) % 16 == 0 &&
-      (p.batch <= 1 || (p.sC * ec) % 16 == 0) && p.ldc * ec < (1LL << 40) &&
-      p.sC * ec < (1LL << 40)) {
+  if (tp.splits > 1) {
+    st = ws_map(&mc, tp);
+    if (st != MM_OK) return st;
+  } else if (!c_trans && (uintptr_t)p.C % 16 == 0 && (p.ldc * ec) % 16 == 0 &&
+             (p.batch <= 1 || (p.sC * ec) % 16 == 0) && p.ldc * ec < (1LL << 40) &&
+             p.sC * ec < (1LL << 40)) {
     st = encode_map(&mc, p.tc, p.C, p.N, p.M, p.batch, p.ldc * ec, p.sC * ec, 128 / ec, 32);
     if (st != MM_OK) return st;
     tp.c_tma = 1;

@@ -186,6 +186,71 @@ def test_gemv_t_rows_chunks(shape, dt):
     c.check(exact=True)
 
 
+TC1 = [i for i, n in enumerate(NAMES) if n.startswith("tc_") and "repack" not in n]
+
+
+@pytest.mark.parametrize("cand", TC1, ids=[NAMES[i] for i in TC1])
+@pytest.mark.parametrize("shape,dt", [((256, 160, 512), (BF16, BF16, F32)),
+                                      ((256, 320, 512), (BF16, BF16, BF16)),
+                                      ((256, 192, 4096), (BF16, BF16, F32))],
+                         ids=["f32-one-box-in-last-tile", "bf16-one-box-in-last-tile",
+                              "splitk-last-box"])
+def test_ragged_n_bulk_store_boxes_repeat(cand, shape, dt):
+    """The epilogue stages output boxes in two alternating buffers and reuses
+    one once its previous bulk store has read it.  Tiles whose last columns
+    fall past N stage fewer boxes; ten launches in a row, each over a fresh
+    NaN-filled output, catch a box refilled while its store still reads it."""
+    c = Case(*shape, layout="NN", dt=dt, dist="int4", seed=sum(shape)).device()
+    for _ in range(10):
+        c.device()
+        st = run(cand, c)
+        if st == mm.MM_ERR_UNSUPPORTED:
+            pytest.skip(mm.mm_last_error())
+        assert st == mm.MM_OK, mm.mm_last_error()
+        c.check(exact=True)
+
+
+@pytest.mark.parametrize("shape,pad,batch", [((4, 42, 3000), (0, 6, 0), 1),
+                                             ((3, 42, 2000), (0, 6, 0), 2),
+                                             ((4, 136, 3000), (0, 0, 5), 1),
+                                             ((5, 33, 1500), (0, 7, 0), 1)],
+                         ids=["groups-cross-rows", "groups-cross-batch", "ldc-padded", "odd-total"])
+def test_splitk_reduce_groups(shape, pad, batch):
+    """The split-K reduction takes four consecutive outputs of the flattened
+    grid a thread when it can: groups that run across a row or a batch item,
+    padded C rows, and an output count that is not a multiple of four (one
+    output a thread).  Every split-K candidate, swapped ones included."""
+    c = Case(*shape, layout="NN", dt=(BF16, BF16, F32), dist="int4", pad=pad, batch=batch,
+             seed=sum(shape)).device()
+    ran = 0
+    for i, n in enumerate(NAMES):
+        if "splitk" not in n:
+            continue
+        c.device()  # a fresh output (and padding) for each candidate
+        st = run(i, c)
+        if st == mm.MM_ERR_UNSUPPORTED:
+            continue
+        assert st == mm.MM_OK, f"{n}: {mm.mm_last_error()}"
+        c.check(exact=True)
+        ran += 1
+    assert ran >= 2
+
+
+@pytest.mark.parametrize("shape,pad,batch", [((40, 72, 5000), (4, 0, 0), 1),
+                                             ((16, 136, 2056), (2, 0, 0), 3),
+                                             ((300, 64, 520), (1, 0, 0), 2)],
+                         ids=["rows-of-two-blocks", "4-byte-pieces-batched", "2-byte-pieces-batched"])
+def test_repack_rows(shape, pad, batch):
+    """A with rows that TMA cannot address is copied to aligned rows first:
+    rows longer than one block's share of pieces, 8-, 4- and 2-byte pieces,
+    several batch items."""
+    i = NAMES.index("tc_repack_128x64")
+    c = Case(*shape, layout="NN", dt=(BF16, BF16, F32), dist="int4", pad=pad, batch=batch,
+             seed=sum(shape)).device()
+    assert run(i, c) == mm.MM_OK, mm.mm_last_error()
+    c.check(exact=True)
+
+
 # ---------------------------------------------------------------- full sizes
 @pytest.mark.parametrize("M", [1, 8, 16])
 @pytest.mark.parametrize("layout", ["NN", "NT"])
