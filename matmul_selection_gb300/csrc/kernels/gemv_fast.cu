@@ -15,18 +15,18 @@
 //       summed in a fixed order: the two rows of a warp by shuffle, the 16 warps
 //       through shared memory, then the 8 CTAs through distributed shared
 //       memory, rank 0..7 in order, each rank finishing CW/8 of the columns.
-//   gemv_n_stream  M = 1, B row-major [K][N], no clusters.  CTA (g, s) covers the
-//       256-byte column group g of the K rows [s*KS, (s+1)*KS), about 256
-//       CTAs in all.  Before the grid waits for its predecessor, each CTA
-//       prefetches its rows of the group into L2 (cp.async.bulk.prefetch.L2):
-//       a prefetch returns nothing to the SM, so it cannot observe a stale
-//       value (the loads after the wait read the coherent L2), and back-to-back
-//       launches keep HBM busy across the kernel boundary.  A clustered grid
-//       cannot start early this way (a cluster needs its GPC's slots free at
-//       once), hence the split sums go to an fp32 workspace and a second,
-//       small kernel adds them in split order (a ticketed last-CTA sum in the
-//       same kernel put ~2 us of serial fence/atomic/reload latency on every
-//       launch's critical path).
+//   gemv_n_stream  M = 1, B row-major [K][N], no clusters.  About two CTAs an
+//       SM: G column groups of 512 bytes x S splits of K, CTA (g, s) streaming
+//       the group's row segments over the rows [s*K/S, (s+1)*K/S).  Before the
+//       grid waits for its predecessor, each CTA prefetches its row segments
+//       into L2 (cp.async.bulk.prefetch.L2): a prefetch returns nothing to the
+//       SM, so it cannot observe a stale value (the loads after the wait read
+//       the coherent L2), and back-to-back launches keep HBM busy across the
+//       kernel boundary.  A clustered grid cannot start early this way (a
+//       cluster needs its GPC's slots free at once), and a second kernel adds a
+//       grid boundary, so the split sums go to an fp32 workspace and the CTA of
+//       the group that arrives last (atomic ticket) adds them in split order,
+//       all its loads of them in flight at once.
 //   gemv_t_rows  B transposed [N][K].  One warp per output column (row of B)
 //       reading the whole row with 16-byte loads; the dot products end in an
 //       xor-shuffle reduction.  No cross-warp or cross-CTA combination.  The
@@ -37,6 +37,7 @@
 #include <cuda_fp16.h>
 
 #include <mutex>
+#include <type_traits>
 
 #include "../common.h"
 
@@ -117,11 +118,19 @@ struct FastArgs {
   int tc;
   int64_t ldc, sC;
   int M, N, K, batch;
-  int KS;  // gemv_n_cluster: rows per cluster rank; gemv_n_stream: rows per split
+  int KS;  // gemv_n_cluster: rows per cluster rank
   // gemv_n_stream
   int G, S;           // column groups, K splits
-  float *ws;          // [batch][G][S][MT][CW] split sums
+  float *ws;          // [batch][G][S][CW] split sums
+  unsigned *tickets;  // [batch][G] arrival counters, zero between calls
 };
+
+// Atomic add with release and acquire semantics at device scope.
+__device__ __forceinline__ unsigned atom_add_acq_rel_gpu(unsigned *p, unsigned v) {
+  unsigned old;
+  asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
 
 // Warm L2 with `bytes` (a multiple of 16) at a 16-byte aligned address.
 __device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes) {
@@ -281,160 +290,135 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1) gemv_n_cluster_kern
 }
 
 // ---------------------------------------------------------------- gemv_n_stream
-// 512 threads with 8 loads in flight a lane (two CTAs an SM): the bytes in
-// flight, not the arithmetic, bound a single pass over B.  With K split the
-// CTAs only write their partial sums; a second small kernel adds them (its
-// launch overlaps this grid's tail, and the next pass over B may start its
-// prefetch while it runs).
+// A CTA of 512 threads streams the 512-byte row segments of its column group
+// over its K rows, a warp per row and four 16-byte loads in flight a lane (more
+// registers a thread would keep the next grid's CTAs off the SM for longer).
+// The S partial sums of a group are combined by whichever of its CTAs finishes
+// last (an atomic ticket), in split order, so the call is a single grid with
+// no second kernel and no serial tail of dependent loads.
 constexpr int kStreamThreads = 512;
-constexpr int kStreamWarps = kStreamThreads / 32;
+constexpr int kStreamU = 4;      // loads in flight a lane
+constexpr int kStreamSegB = 512; // bytes of a row segment (one warp, 16 bytes a lane)
 
-template <int MT, int TB>
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+__device__ __forceinline__ float to_f32(__half x) { return __half2float(x); }
+
+// The main loop of gemv_n_stream: this lane's 16 bytes of every RPS-th row of
+// the CTA's rows, kStreamU loads in flight.  A lane whose first column is
+// inside the matrix loads its whole 16-byte piece: rows are 16-byte aligned,
+// so the piece cannot cross a page, and the columns past N it picks up (row
+// padding, or bytes past the operand's last row) only feed sums that are
+// never stored.  Lanes past N load nothing.
+template <int TB, int TA>
+__device__ __forceinline__ void stream_rows(const char *Bk, int64_t ldb, bool lane_in, int col,
+                                            const void *A, int64_t a0, int64_t a_cs, int rr, int kr,
+                                            float *acc) {
+  constexpr int EB = TB == MM_F32 ? 4 : 2;
+  constexpr int VEC = 16 / EB;
+  constexpr int RPS = kStreamThreads / 32;
+  using TAe = typename std::conditional<TA == MM_F32, float,
+              typename std::conditional<TA == MM_BF16, __nv_bfloat16, __half>::type>::type;
+  const int64_t step = ldb * EB * RPS;
+  const char *rp = Bk + (int64_t)rr * ldb * EB + (int64_t)col * EB;
+  const TAe *ap = static_cast<const TAe *>(A) + a0 + (int64_t)rr * a_cs;
+  const int64_t astep = a_cs * RPS;
+  for (int r0 = rr; r0 < kr; r0 += RPS * kStreamU) {
+    uint4 v[kStreamU];
+    float a[kStreamU];
+#pragma unroll
+    for (int u = 0; u < kStreamU; ++u) {
+      const bool in = r0 + u * RPS < kr;
+      v[u] = in && lane_in ? __ldcs(reinterpret_cast<const uint4 *>(rp + u * step)) : make_uint4(0, 0, 0, 0);
+      a[u] = in ? to_f32(ap[u * astep]) : 0.f;
+    }
+    rp += kStreamU * step;
+    ap += kStreamU * astep;
+#pragma unroll
+    for (int u = 0; u < kStreamU; ++u) {
+      float bf[VEC];
+      unpack16<TB>(v[u], bf);
+#pragma unroll
+      for (int j = 0; j < VEC; ++j) acc[j] = fmaf(a[u], bf[j], acc[j]);
+    }
+  }
+}
+
+template <int TB, int TA>
 __global__ void __launch_bounds__(kStreamThreads, 2) gemv_n_stream_kernel(const FastArgs g) {
   pdl_launch_dependents();
   constexpr int EB = TB == MM_F32 ? 4 : 2;
   constexpr int VEC = 16 / EB;
-  constexpr int CW = 256 / EB;          // columns per group: 256 bytes of a row
-  constexpr int LPR = CW / VEC;         // 16 lanes per row segment
-  constexpr int RPW = 32 / LPR;         // 2 rows per warp instruction
-  constexpr int STEP = kStreamWarps * RPW;    // 32 rows per step
-  constexpr int U = 8;                  // loads in flight per lane
-  constexpr int APT = MT;               // A elements a thread preloads (slices of <= 512 rows)
-  extern __shared__ float fsm[];
-  float *As = fsm;                      // [KS][MT]
-  float *part = fsm + g.KS * MT;        // [warps][MT][CW]
-  const int grp = blockIdx.x, sp = blockIdx.y, b = blockIdx.z;
-  const int k0 = sp * g.KS;
-  const int kr = max(0, min(g.KS, g.K - k0));
-  const char *Bb = g.B + (int64_t)b * g.sB * EB;
-  {  // this CTA's rows of the column group, whole 16-byte pieces
-    const int64_t run = ((int64_t)min(CW, g.N - grp * CW) * EB) & ~(int64_t)15;
+  constexpr int CW = kStreamSegB / EB;              // columns of a group
+  constexpr int RPS = kStreamThreads / 32;          // rows per step: one a warp
+  constexpr int H = kStreamThreads / CW;            // threads per column in the final sum
+  extern __shared__ float part[];                   // [RPS][CW], then [H][CW]
+  __shared__ unsigned last;
+  const int b = blockIdx.y;
+  const int grp = blockIdx.x / g.S, sp = blockIdx.x - grp * g.S;
+  const int k0 = (int)((int64_t)sp * g.K / g.S);
+  const int kr = (int)((int64_t)(sp + 1) * g.K / g.S) - k0;
+  const int col0 = grp * CW;
+  const char *Bk = g.B + ((int64_t)b * g.sB + (int64_t)k0 * g.ldb) * EB;  // row k0, column 0
+  {  // this CTA's row segments, whole 16-byte pieces, into L2 before the wait
+    const int64_t run = ((int64_t)min(CW, g.N - col0) * EB) & ~(int64_t)15;
     if (run > 0)
       for (int r = threadIdx.x; r < kr; r += kStreamThreads)
-        prefetch_l2(Bb + ((int64_t)(k0 + r) * g.ldb + (int64_t)grp * CW) * EB, (uint32_t)run);
+        prefetch_l2(Bk + ((int64_t)r * g.ldb + col0) * EB, (uint32_t)run);
   }
-  pdl_wait();  // A, the workspace and C only after the previous kernel completed
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int sub = lane / LPR, li = lane % LPR;
-  const int col = grp * CW + li * VEC;
-  // this thread's elements of A's slice: issued first, stored after B's first loads
-  const int na = g.KS * MT;
-  float areg[APT];
+  pdl_wait();  // A, the workspace, the tickets and C only after the previous kernel
+  const int lane = threadIdx.x & 31, rr = threadIdx.x >> 5;
+  const int col = col0 + lane * VEC;
+  const int64_t a0 = (int64_t)b * g.sA + (int64_t)k0 * g.a_cs;
+  float acc[VEC];
 #pragma unroll
-  for (int u = 0; u < APT; ++u) {
-    const int e = threadIdx.x + u * kStreamThreads;
-    const int kk = e / MT, m = e - kk * MT;
-    areg[u] = (e < na && m < g.M && kk < kr)
-                  ? ld_any(g.A, (int64_t)b * g.sA + (int64_t)m * g.a_rs + (int64_t)(k0 + kk) * g.a_cs,
-                           g.ta)
-                  : 0.f;
-  }
-  float acc[MT][VEC];
+  for (int j = 0; j < VEC; ++j) acc[j] = 0.f;
+  stream_rows<TB, TA>(Bk, g.ldb, col < g.N, col, g.A, a0, g.a_cs, rr, kr, acc);
+  // the CTA's rows, added in row-phase order
 #pragma unroll
-  for (int m = 0; m < MT; ++m)
-#pragma unroll
-    for (int j = 0; j < VEC; ++j) acc[m][j] = 0.f;
-  bool staged = false;
-  for (int r0 = warp * RPW + sub; r0 < g.KS; r0 += STEP * U) {
-    uint4 v[U];
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int r = r0 + u * STEP;
-      v[u] = (r < kr) ? load16<TB>(Bb + (int64_t)(k0 + r) * g.ldb * EB, col, g.N)
-                      : make_uint4(0, 0, 0, 0);
-    }
-    if (!staged) {  // B's first loads are in flight; now publish A's slice
-#pragma unroll
-      for (int u = 0; u < APT; ++u) {
-        const int e = threadIdx.x + u * kStreamThreads;
-        if (e < na) As[e] = areg[u];
-      }
-      for (int e = threadIdx.x + APT * kStreamThreads; e < na; e += kStreamThreads) {  // slices > 512 rows
-        const int kk = e / MT, m = e - kk * MT;
-        As[e] = (m < g.M && kk < kr) ? ld_any(g.A, (int64_t)b * g.sA + (int64_t)m * g.a_rs +
-                                                       (int64_t)(k0 + kk) * g.a_cs, g.ta)
-                                     : 0.f;
-      }
-      __syncthreads();
-      staged = true;
-    }
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int r = r0 + u * STEP;
-      if (r < kr) {
-        float bf[VEC];
-        unpack16<TB>(v[u], bf);
-        const float *a = As + r * MT;
-#pragma unroll
-        for (int m = 0; m < MT; ++m)
-#pragma unroll
-          for (int j = 0; j < VEC; ++j) acc[m][j] = fmaf(a[m], bf[j], acc[m][j]);
-      }
-    }
-  }
-  // rows of a warp: fixed-order xor shuffle over the RPW row lanes
-#pragma unroll
-  for (int m = 0; m < MT; ++m)
-#pragma unroll
-    for (int j = 0; j < VEC; ++j) {
-      float x = acc[m][j];
-#pragma unroll
-      for (int o = LPR; o < 32; o <<= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
-      acc[m][j] = x;
-    }
-  if (sub == 0)
-#pragma unroll
-    for (int m = 0; m < MT; ++m)
-#pragma unroll
-      for (int j = 0; j < VEC; ++j) part[(warp * MT + m) * CW + li * VEC + j] = acc[m][j];
+  for (int j = 0; j < VEC; ++j) part[rr * CW + lane * VEC + j] = acc[j];
   __syncthreads();
-  // the CTA's sum over its warps in order
-  constexpr int PER = (MT * CW + kStreamThreads - 1) / kStreamThreads;
-  float cta[PER];
+  const int c = threadIdx.x % CW;
+  float t = 0.f;
+  if (threadIdx.x < CW)
 #pragma unroll
-  for (int q = 0; q < PER; ++q) {
-    const int e = threadIdx.x + q * kStreamThreads;
-    float t = 0.f;
-    if (e < MT * CW)
-      for (int w = 0; w < kStreamWarps; ++w) t += part[w * MT * CW + e];
-    cta[q] = t;
-  }
+    for (int q = 0; q < RPS; ++q) t += part[q * CW + c];
   if (g.S == 1) {
-#pragma unroll
-    for (int q = 0; q < PER; ++q) {
-      const int e = threadIdx.x + q * kStreamThreads;
-      const int m = e / CW, n = grp * CW + (e - m * CW);
-      if (e < MT * CW && m < g.M && n < g.N)
-        st_any(g.C, (int64_t)b * g.sC + (int64_t)m * g.ldc + n, g.tc, cta[q]);
-    }
+    if (threadIdx.x < CW && col0 + c < g.N) st_any(g.C, (int64_t)b * g.sC + col0 + c, g.tc, t);
     return;
   }
-  float *ws_part = g.ws + (((int64_t)b * g.G + grp) * g.S + sp) * (MT * CW);
+  const int64_t tile = (int64_t)b * g.G + grp;
+  float *ws = g.ws + tile * g.S * CW;  // [S][CW] of this group
+  if (threadIdx.x < CW) __stcg(ws + (int64_t)sp * CW + c, t);
+  // The barrier orders every thread's partial store before thread 0's
+  // release; thread 0's acquire (in the last CTA) orders the other CTAs'
+  // partials before this CTA's loads, which the second barrier extends to
+  // all of its threads.
+  __syncthreads();
+  if (threadIdx.x == 0) last = atom_add_acq_rel_gpu(g.tickets + tile, 1u) == (unsigned)g.S - 1;
+  __syncthreads();
+  if (!last) return;
+  // H threads a column: thread h adds the splits [h*S/H, (h+1)*S/H) with all of
+  // their loads in flight, then the H run sums are added in run order.
+  const int h = threadIdx.x / CW;
+  const int sb = h * g.S / H, se = (h + 1) * g.S / H;
+  float run = 0.f;
+  for (int s0 = sb; s0 < se; s0 += 16) {
+    float x[16];
 #pragma unroll
-  for (int q = 0; q < PER; ++q) {
-    const int e = threadIdx.x + q * kStreamThreads;
-    if (e < MT * CW) __stcg(ws_part + e, cta[q]);
+    for (int q = 0; q < 16; ++q) x[q] = s0 + q < se ? __ldcg(ws + (int64_t)(s0 + q) * CW + c) : 0.f;
+#pragma unroll
+    for (int q = 0; q < 16; ++q) run += x[q];
   }
-}
-
-// The split sums of gemv_n_stream, added in split order: one thread per
-// output element.
-template <int MT, int CW>
-__global__ void __launch_bounds__(256) gemv_stream_reduce_kernel(const FastArgs g) {
-  pdl_launch_dependents();
-  pdl_wait();
-  const int64_t total = (int64_t)g.batch * g.G * MT * CW;
-  for (int64_t x = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; x < total;
-       x += (int64_t)gridDim.x * blockDim.x) {
-    const int e = (int)(x % (MT * CW));
-    const int64_t tile = x / (MT * CW);  // b * G + grp
-    const int grp = (int)(tile % g.G), b = (int)(tile / g.G);
-    const int m = e / CW, n = grp * CW + (e - m * CW);
-    const float *p = g.ws + tile * g.S * (MT * CW) + e;
-    float t = 0.f;
-    for (int q = 0; q < g.S; ++q) t += __ldcg(p + (int64_t)q * MT * CW);
-    if (m < g.M && n < g.N) st_any(g.C, (int64_t)b * g.sC + (int64_t)m * g.ldc + n, g.tc, t);
+  part[h * CW + c] = run;
+  __syncthreads();
+  if (threadIdx.x < CW) {
+    float y = 0.f;
+#pragma unroll
+    for (int q = 0; q < H; ++q) y += part[q * CW + c];
+    if (col0 + c < g.N) st_any(g.C, (int64_t)b * g.sC + col0 + c, g.tc, y);
   }
+  if (threadIdx.x == 0) g.tickets[tile] = 0;  // ready for the next call on this stream
 }
 
 // ---------------------------------------------------------------- gemv_t_rows
@@ -549,21 +533,18 @@ const FastCfg kFastCfgs[] = {
     {"gemv_n_cluster", false, false}, {"gemv_t_rows", true, false}, {"gemv_n_stream", false, true}};
 
 constexpr int kStreamMaxM = 1;
-constexpr int kStreamMaxRows = 2048;
-constexpr int64_t kStreamTargetCtas = 256;
+constexpr int64_t kStreamMaxSplits = 64;
 
-// gemv_n_stream geometry: column groups, K splits and rows per split so that
-// the grid holds about kStreamTargetCtas CTAs.
-void stream_plan(int64_t N, int64_t K, int64_t batch, int eb, int64_t *G, int64_t *S, int *KS) {
-  const int64_t cw = 256 / eb;
+// gemv_n_stream geometry: column groups of 512 bytes and K splits so that the
+// grid holds about two CTAs per SM (a whole number per SM keeps every SM's
+// share of the bytes equal).
+void stream_plan(int64_t N, int64_t K, int64_t batch, int eb, int sms, int64_t *G, int64_t *S) {
+  const int64_t cw = kStreamSegB / eb;
   *G = (N + cw - 1) / cw;
-  int64_t s = (kStreamTargetCtas + *G * batch - 1) / (*G * batch);
-  if (s < 1) s = 1;
-  int64_t ks = (K + s - 1) / s;
-  ks = (ks + 31) / 32 * 32;
-  if (ks > kStreamMaxRows) ks = kStreamMaxRows;
-  *KS = (int)ks;
-  *S = (K + ks - 1) / ks;
+  const int64_t tiles = *G * batch;
+  int64_t s = (2 * (int64_t)sms + tiles / 2) / tiles;
+  s = std::max<int64_t>(1, std::min<int64_t>(s, std::min<int64_t>(K, kStreamMaxSplits)));
+  *S = s;
 }
 
 int mt_of(int64_t M) { return M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : 8; }
@@ -577,9 +558,7 @@ size_t smem_n(int mt, int ks, int eb) {
 // gemv_t_rows: A as fp32 rows padded to whole 512-byte chunks of B (at most
 // 256 elements a chunk).
 size_t smem_t(int mt, int64_t K) { return (size_t)mt * ((K + 255) / 256 * 256) * sizeof(float); }
-size_t smem_stream(int mt, int ks, int eb) {
-  return ((size_t)ks * mt + (size_t)kStreamWarps * mt * (256 / eb)) * sizeof(float);
-}
+size_t smem_stream(int eb) { return (size_t)(kStreamThreads / 32) * (kStreamSegB / eb) * sizeof(float); }
 
 int rows_per_rank(int64_t K) {
   int64_t ks = (K + kCluster - 1) / kCluster;
@@ -618,26 +597,18 @@ mm_status launch_t(const FastArgs &g, size_t smem, cudaStream_t s) {
   return e == cudaSuccess ? MM_OK : cuda_error(e, "gemv_t_rows launch");
 }
 
-template <int MT, int TB>
+template <int TB, int TA>
 mm_status launch_stream(const FastArgs &g, size_t smem, cudaStream_t s) {
-  auto kern = gemv_n_stream_kernel<MT, TB>;
-  cudaError_t e;
-  e = smem_attr(kern, smem);
-  if (e != cudaSuccess) return cuda_error(e, "gemv_n_stream smem attribute");
-  e = launch_pdl(kern, dim3((unsigned)g.G, (unsigned)g.S, (unsigned)g.batch), dim3(kStreamThreads),
-                 smem, s, dim3(1), g);
-  if (e != cudaSuccess) return cuda_error(e, "gemv_n_stream launch");
-  if (g.S == 1) return MM_OK;
-  constexpr int CW = TB == MM_F32 ? 64 : 128;
-  const int64_t total = (int64_t)g.batch * g.G * MT * CW;
-  const int blocks = (int)std::min<int64_t>((total + 255) / 256, 4096);
-  e = launch_pdl(gemv_stream_reduce_kernel<MT, CW>, dim3(blocks), dim3(256), 0, s, dim3(1), g);
-  return e == cudaSuccess ? MM_OK : cuda_error(e, "gemv_stream_reduce launch");
+  cudaError_t e = launch_pdl(gemv_n_stream_kernel<TB, TA>, dim3((unsigned)(g.G * g.S), (unsigned)g.batch),
+                             dim3(kStreamThreads), smem, s, dim3(1), g);
+  return e == cudaSuccess ? MM_OK : cuda_error(e, "gemv_n_stream launch");
 }
 
 template <int TB>
-mm_status launch_stream_tb(int, const FastArgs &g, size_t smem, cudaStream_t s) {
-  return launch_stream<1, TB>(g, smem, s);
+mm_status launch_stream_ta(const FastArgs &g, size_t smem, cudaStream_t s) {
+  if (g.ta == MM_BF16) return launch_stream<TB, MM_BF16>(g, smem, s);
+  if (g.ta == MM_F16) return launch_stream<TB, MM_F16>(g, smem, s);
+  return launch_stream<TB, MM_F32>(g, smem, s);
 }
 
 template <int TB>
@@ -675,10 +646,9 @@ bool gemv_fast_supports(const Problem &p, const DeviceInfo &d, int cfg, std::str
   if (c.stream) {
     if (p.M > kStreamMaxM) return no("M must be 1");
     int64_t G, S;
-    int KS;
-    stream_plan(p.N, p.K, p.batch, eb, &G, &S, &KS);
-    if (G >= (1LL << 31) || S > 65535) return no("too many column groups or splits");
-    smem = smem_stream(mt, KS, eb);
+    stream_plan(p.N, p.K, p.batch, eb, d.sms, &G, &S);
+    if (G * S >= (1LL << 31)) return no("too many column groups");
+    smem = smem_stream(eb);
   } else {
     smem = c.b_trans ? smem_t(mt, p.K) : smem_n(mt, rows_per_rank(p.K), eb);
   }
@@ -714,21 +684,24 @@ mm_status launch_gemv_fast(const Problem &p, LaunchCtx &ctx, int cfg) {
   size_t smem;
   if (c.stream) {
     int64_t G, S;
-    stream_plan(p.N, p.K, p.batch, eb, &G, &S, &g.KS);
+    stream_plan(p.N, p.K, p.batch, eb, ctx.dev->info.sms, &G, &S);
     g.G = (int)G;
     g.S = (int)S;
-    smem = smem_stream(mt, g.KS, eb);
+    smem = smem_stream(eb);
     if (S > 1) {
-      const size_t cw = 256 / eb;
-      const size_t ws_bytes = (size_t)p.batch * G * S * mt * cw * sizeof(float);
-      void *w = nullptr;
+      const size_t ws_bytes = (size_t)p.batch * G * S * (kStreamSegB / eb) * sizeof(float);
+      const size_t tickets_bytes = (size_t)p.batch * G * sizeof(unsigned);
+      void *w = nullptr, *t = nullptr;
       mm_status st = get_scratch(*ctx.dev, ctx.stream, SCRATCH_WORKSPACE, ws_bytes, &w);
       if (st != MM_OK) return st;
+      st = get_scratch(*ctx.dev, ctx.stream, SCRATCH_TICKETS, tickets_bytes, &t);
+      if (st != MM_OK) return st;
       g.ws = static_cast<float *>(w);
+      g.tickets = static_cast<unsigned *>(t);
     }
-    if (p.tb == MM_BF16) return launch_stream_tb<MM_BF16>(mt, g, smem, ctx.stream);
-    if (p.tb == MM_F16) return launch_stream_tb<MM_F16>(mt, g, smem, ctx.stream);
-    return launch_stream_tb<MM_F32>(mt, g, smem, ctx.stream);
+    if (p.tb == MM_BF16) return launch_stream_ta<MM_BF16>(g, smem, ctx.stream);
+    if (p.tb == MM_F16) return launch_stream_ta<MM_F16>(g, smem, ctx.stream);
+    return launch_stream_ta<MM_F32>(g, smem, ctx.stream);
   }
   if (!c.b_trans) {
     g.KS = rows_per_rank(p.K);

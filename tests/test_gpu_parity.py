@@ -153,13 +153,16 @@ def test_results_deterministic():
 
 
 @pytest.mark.parametrize("shape", [(1, 4096, 4096), (1, 1000, 700), (1, 136, 5000), (1, 64, 33),
-                                   (1, 8, 20000)], ids=lambda s: "x".join(map(str, s)))
+                                   (1, 8, 20000), (1, 81920, 40), (1, 4104, 3)],
+                         ids=lambda s: "x".join(map(str, s)))
 @pytest.mark.parametrize("dt", [(BF16, BF16, F32), (F16, F16, F16), (F32, F32, F32)],
                          ids=["bf16-f32", "f16-f16", "f32-f32"])
 def test_gemv_n_stream_splits(shape, dt):
-    """The split-K GEMV whose split sums a second kernel adds: single and
-    many K splits, a ragged last column group, and three launches in a row
-    over a fresh output each time."""
+    """The split-K GEMV whose split sums the last-arriving CTA of each column
+    group adds: one split (wide N), as many splits as K rows, the split cap
+    (narrow N, long K), a ragged last column group, and three launches in a
+    row over a fresh output each time (the arrival counters must be back at
+    zero after every call)."""
     i = NAMES.index("gemv_n_stream")
     c = Case(*shape, layout="NN", dt=dt, dist="int4", seed=sum(shape)).device()
     for _ in range(3):
