@@ -249,7 +249,7 @@ def kernel_sources(kernel_name):
         names = ["repack.cu", "tc_gemm.cu"]
     elif kernel_name.startswith(("tc", "gemv_swap_tc")):
         names = ["tc_gemm.cu"]
-    elif kernel_name in ("gemv_n_cluster", "gemv_t_rows", "gemv_n_stream"):
+    elif kernel_name in ("gemv_n_cluster", "gemv_t_rows", "gemv_n_stream", "gemv_t_stream"):
         names = ["gemv_fast.cu"]
     elif kernel_name.startswith("gemv"):
         names = ["gemv.cu"]

@@ -136,22 +136,34 @@ __device__ void finish_tile(const GemvArgs &g, int b, int tile, int s, int col0,
     int m = e / ncols, j = e - m * ncols, n = col0 + j;
     if (m < g.M && n < g.N) __stcg(ws_s + (int64_t)m * g.N + n, blockpart[e]);
   }
-  __threadfence();
+  // The barrier orders every thread's partial store before thread 0's
+  // release; thread 0's acquire in the last block orders the other blocks'
+  // partials before this block's loads (the second barrier extends it).
   __syncthreads();
   __shared__ int last;
   if (threadIdx.x == 0) {
-    unsigned prev = atomicAdd(&g.tickets[b * g.n_tiles + tile], 1u);
+    unsigned prev;
+    asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], %2;"
+                 : "=r"(prev)
+                 : "l"(&g.tickets[b * g.n_tiles + tile]), "r"(1u)
+                 : "memory");
     last = (prev == (unsigned)g.S - 1);
   }
   __syncthreads();
   if (!last) return;
-  __threadfence();
   for (int e = threadIdx.x; e < MT * ncols; e += kThreads) {
     int m = e / ncols, j = e - m * ncols, n = col0 + j;
     if (m < g.M && n < g.N) {
+      const float *p = g.ws + (int64_t)b * MN + (int64_t)m * g.N + n;
+      const int64_t sstride = (int64_t)g.batch * MN;
       float sum = 0.f;
-      for (int t = 0; t < g.S; ++t)
-        sum += __ldcg(g.ws + ((int64_t)t * g.batch + b) * MN + (int64_t)m * g.N + n);
+      for (int t0 = 0; t0 < g.S; t0 += 8) {  // splits in order, 8 loads in flight
+        float x[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) x[q] = t0 + q < g.S ? __ldcg(p + (int64_t)(t0 + q) * sstride) : 0.f;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) sum += x[q];
+      }
       st_elem(g.C, b * g.sC + (int64_t)m * g.ldc + n, g.tc, sum);
     }
   }

@@ -421,6 +421,95 @@ __global__ void __launch_bounds__(kStreamThreads, 2) gemv_n_stream_kernel(const 
   if (threadIdx.x == 0) g.tickets[tile] = 0;  // ready for the next call on this stream
 }
 
+// ---------------------------------------------------------------- gemv_t_stream
+// M = 1, B transposed (stored [N][K]): output n is the dot product of A with
+// the contiguous row n of B, so a CTA can own whole rows and no CTA depends on
+// another.  CTA c of about two per SM takes the rows [c*N/C, (c+1)*N/C)
+// (prefetched into L2 before the grid dependency wait); thread t holds the
+// 16-byte pieces t, t+512, ... of every row (a warp reads 512 contiguous bytes
+// of a row) against A's matching elements, four rows of loads in flight, one
+// partial dot product per row of a block of 16 rows.  Each block is summed
+// across the CTA in a fixed order (xor shuffles in a warp, then the 16 warps
+// in order) and written.
+constexpr int kTsThreads = 512;
+constexpr int kTsRB = 16;  // rows per block
+constexpr int kTsU = 4;    // rows of loads in flight
+
+template <int TB, int TA>
+__global__ void __launch_bounds__(kTsThreads, 2) gemv_t_stream_kernel(const FastArgs g) {
+  pdl_launch_dependents();
+  constexpr int EB = TB == MM_F32 ? 4 : 2;
+  constexpr int VEC = 16 / EB;
+  constexpr int W = kTsThreads / 32;
+  using TAe = typename std::conditional<TA == MM_F32, float,
+              typename std::conditional<TA == MM_BF16, __nv_bfloat16, __half>::type>::type;
+  __shared__ float red[W][kTsRB];
+  const int b = blockIdx.y;
+  const int C = gridDim.x, c = blockIdx.x;
+  const int r0 = (int)((int64_t)c * g.N / C), r1 = (int)((int64_t)(c + 1) * g.N / C);
+  const char *Bb = g.B + (int64_t)b * g.sB * EB;
+  const int64_t rowb = g.ldb * EB;
+  {  // this CTA's rows, whole 16-byte pieces, into L2 before the wait
+    const int64_t run = ((int64_t)g.K * EB) & ~(int64_t)15;
+    for (int r = r0 + (int)threadIdx.x; r < r1 && run > 0; r += kTsThreads)
+      for (int64_t o = 0; o < run; o += 65536)
+        prefetch_l2(Bb + (int64_t)r * rowb + o, (uint32_t)(run - o < 65536 ? run - o : 65536));
+  }
+  pdl_wait();
+  const TAe *Ab = static_cast<const TAe *>(g.A) + (int64_t)b * g.sA;
+  const int ppr = (g.K + VEC - 1) / VEC;  // 16-byte pieces of a row
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int rb = r0; rb < r1; rb += kTsRB) {
+    float acc[kTsRB];
+#pragma unroll
+    for (int i = 0; i < kTsRB; ++i) acc[i] = 0.f;
+    for (int p = threadIdx.x; p < ppr; p += kTsThreads) {
+      const int kb = p * VEC;
+      const bool tail = kb + VEC > g.K;  // the last piece of a row: elements past K are not B's
+      float a[VEC];
+#pragma unroll
+      for (int q = 0; q < VEC; ++q) a[q] = kb + q < g.K ? to_f32(Ab[(int64_t)(kb + q) * g.a_cs]) : 0.f;
+      const char *bp = Bb + (int64_t)rb * rowb + (int64_t)kb * EB;
+#pragma unroll
+      for (int i0 = 0; i0 < kTsRB; i0 += kTsU) {
+        uint4 v[kTsU];
+#pragma unroll
+        for (int u = 0; u < kTsU; ++u)
+          v[u] = rb + i0 + u < r1 ? __ldcs(reinterpret_cast<const uint4 *>(bp + (int64_t)(i0 + u) * rowb))
+                                  : make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int u = 0; u < kTsU; ++u) {
+          float bf[VEC];
+          unpack16<TB>(v[u], bf);
+          if (tail)
+#pragma unroll
+            for (int q = 0; q < VEC; ++q) bf[q] = kb + q < g.K ? bf[q] : 0.f;
+#pragma unroll
+          for (int q = 0; q < VEC; ++q) acc[i0 + u] = fmaf(a[q], bf[q], acc[i0 + u]);
+        }
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < kTsRB; ++i) {
+      float x = acc[i];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+      acc[i] = x;
+    }
+    if (lane == 0)
+#pragma unroll
+      for (int i = 0; i < kTsRB; ++i) red[warp][i] = acc[i];
+    __syncthreads();
+    if (threadIdx.x < kTsRB && rb + (int)threadIdx.x < r1) {
+      float t = 0.f;
+#pragma unroll
+      for (int w = 0; w < W; ++w) t += red[w][threadIdx.x];
+      st_any(g.C, (int64_t)b * g.sC + rb + threadIdx.x, g.tc, t);
+    }
+    __syncthreads();  // red is reused by the next block
+  }
+}
+
 // ---------------------------------------------------------------- gemv_t_rows
 // A warp walks its row of B in chunks of CE = 32 * VEC elements (512 bytes),
 // lane l holding elements [l * VEC, (l + 1) * VEC) of a chunk.  A sits in
@@ -530,7 +619,8 @@ struct FastCfg {
   bool stream;  // gemv_n_stream
 };
 const FastCfg kFastCfgs[] = {
-    {"gemv_n_cluster", false, false}, {"gemv_t_rows", true, false}, {"gemv_n_stream", false, true}};
+    {"gemv_n_cluster", false, false}, {"gemv_t_rows", true, false}, {"gemv_n_stream", false, true},
+    {"gemv_t_stream", true, true}};
 
 constexpr int kStreamMaxM = 1;
 constexpr int64_t kStreamMaxSplits = 64;
@@ -558,6 +648,12 @@ size_t smem_n(int mt, int ks, int eb) {
 // gemv_t_rows: A as fp32 rows padded to whole 512-byte chunks of B (at most
 // 256 elements a chunk).
 size_t smem_t(int mt, int64_t K) { return (size_t)mt * ((K + 255) / 256 * 256) * sizeof(float); }
+// gemv_t_stream: CTAs per batch item, about two per SM, at least one row each.
+int64_t tstream_ctas(int64_t N, int64_t batch, int sms) {
+  const int64_t per = (2 * (int64_t)sms + batch - 1) / batch;
+  return std::max<int64_t>(1, std::min<int64_t>(N, per));
+}
+
 size_t smem_stream(int eb) { return (size_t)(kStreamThreads / 32) * (kStreamSegB / eb) * sizeof(float); }
 
 int rows_per_rank(int64_t K) {
@@ -604,6 +700,20 @@ mm_status launch_stream(const FastArgs &g, size_t smem, cudaStream_t s) {
   return e == cudaSuccess ? MM_OK : cuda_error(e, "gemv_n_stream launch");
 }
 
+template <int TB, int TA>
+mm_status launch_tstream(const FastArgs &g, int64_t C, cudaStream_t s) {
+  cudaError_t e = launch_pdl(gemv_t_stream_kernel<TB, TA>, dim3((unsigned)C, (unsigned)g.batch),
+                             dim3(kTsThreads), 0, s, dim3(1), g);
+  return e == cudaSuccess ? MM_OK : cuda_error(e, "gemv_t_stream launch");
+}
+
+template <int TB>
+mm_status launch_tstream_ta(const FastArgs &g, int64_t C, cudaStream_t s) {
+  if (g.ta == MM_BF16) return launch_tstream<TB, MM_BF16>(g, C, s);
+  if (g.ta == MM_F16) return launch_tstream<TB, MM_F16>(g, C, s);
+  return launch_tstream<TB, MM_F32>(g, C, s);
+}
+
 template <int TB>
 mm_status launch_stream_ta(const FastArgs &g, size_t smem, cudaStream_t s) {
   if (g.ta == MM_BF16) return launch_stream<TB, MM_BF16>(g, smem, s);
@@ -645,10 +755,14 @@ bool gemv_fast_supports(const Problem &p, const DeviceInfo &d, int cfg, std::str
   size_t smem;
   if (c.stream) {
     if (p.M > kStreamMaxM) return no("M must be 1");
-    int64_t G, S;
-    stream_plan(p.N, p.K, p.batch, eb, d.sms, &G, &S);
-    if (G * S >= (1LL << 31)) return no("too many column groups");
-    smem = smem_stream(eb);
+    if (c.b_trans) {
+      smem = 0;
+    } else {
+      int64_t G, S;
+      stream_plan(p.N, p.K, p.batch, eb, d.sms, &G, &S);
+      if (G * S >= (1LL << 31)) return no("too many column groups");
+      smem = smem_stream(eb);
+    }
   } else {
     smem = c.b_trans ? smem_t(mt, p.K) : smem_n(mt, rows_per_rank(p.K), eb);
   }
@@ -682,6 +796,12 @@ mm_status launch_gemv_fast(const Problem &p, LaunchCtx &ctx, int cfg) {
   g.batch = (int)p.batch;
   int groups = 0;
   size_t smem;
+  if (c.stream && c.b_trans) {
+    const int64_t C = tstream_ctas(p.N, p.batch, ctx.dev->info.sms);
+    if (p.tb == MM_BF16) return launch_tstream_ta<MM_BF16>(g, C, ctx.stream);
+    if (p.tb == MM_F16) return launch_tstream_ta<MM_F16>(g, C, ctx.stream);
+    return launch_tstream_ta<MM_F32>(g, C, ctx.stream);
+  }
   if (c.stream) {
     int64_t G, S;
     stream_plan(p.N, p.K, p.batch, eb, ctx.dev->info.sms, &G, &S);

@@ -101,6 +101,7 @@ def test_every_candidate_runs_somewhere():
         "gemv_n_cluster": Case(4, 1000, 520, layout="NN", dist="int4"),
         "gemv_t_rows": Case(3, 300, 1000, layout="NT", dist="int4"),
         "gemv_n_stream": Case(1, 1000, 700, layout="NN", dist="int4"),
+        "gemv_t_stream": Case(1, 1000, 704, layout="NT", dist="int4"),
         "tc2_repack_256x256": Case(300, 264, 200, layout="NN", dist="int4", pad=(4, 0, 0)),
         "tc_repack_128x128": Case(300, 264, 200, layout="TN", dist="int4", pad=(3, 0, 0)),
         "tc_repack_128x64": Case(130, 72, 136, layout="NT", dist="int4", pad=(0, 5, 0)),
@@ -150,6 +151,33 @@ def test_results_deterministic():
         r1 = c.result().copy()
         assert run(i, c) == mm.MM_OK
         assert np.array_equal(r1.view(np.uint8), c.result().view(np.uint8)), NAMES[i]
+
+
+@pytest.mark.parametrize("shape_pad", [((1, 4096, 4096), 0), ((1, 1000, 700), 4), ((1, 5, 20000), 0),
+                                       ((1, 70000, 24), 0), ((1, 300, 4100), 4), ((1, 77, 3), 5)],
+                         ids=lambda s: "x".join(map(str, s[0])) + f"+{s[1]}")
+@pytest.mark.parametrize("dt", [(BF16, BF16, F32), (F16, F16, F16), (F32, F32, F32)],
+                         ids=["bf16-f32", "f16-f16", "f32-f32"])
+def test_gemv_t_stream_rows(shape_pad, dt):
+    """The transposed-B M=1 GEMV that gives each CTA whole rows of B: fewer
+    rows than CTAs, many row blocks a CTA (wide N), K not a multiple of the
+    16-byte piece with NaN-filled row padding right after it (elements past K
+    must not reach the sums), three launches in a row over a fresh output."""
+    shape, pad = shape_pad
+    i = NAMES.index("gemv_t_stream")
+    c = Case(*shape, layout="NT", dt=dt, dist="int4", pad=(0, pad, 0), seed=sum(shape)).device()
+    for _ in range(3):
+        c.device()
+        assert run(i, c) == mm.MM_OK, mm.mm_last_error()
+        c.check(exact=True)
+    # batch gaps that keep every B item 16-byte aligned
+    cb = Case(1, 296, 900, layout="NT", dt=dt, dist="int4", batch=3, bstride_extra=(8, 20, 8),
+              pad=(8, 4, 4)).device()
+    assert run(i, cb) == mm.MM_OK, mm.mm_last_error()
+    cb.check(exact=True)
+    cr = Case(1, 4096, 4096, layout="NT", dt=dt, dist="normal", seed=5).device()
+    assert run(i, cr) == mm.MM_OK, mm.mm_last_error()
+    cr.check(exact=False)
 
 
 @pytest.mark.parametrize("shape", [(1, 4096, 4096), (1, 1000, 700), (1, 136, 5000), (1, 64, 33),
