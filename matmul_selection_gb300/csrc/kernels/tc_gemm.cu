@@ -193,6 +193,28 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *map
       : "memory");
 }
 
+// L2 prefetch of one box of a tensor map: no shared memory, no barrier, and
+// nothing returned to the SM, so it may run before the grid dependency wait
+// (it cannot observe a value the previous kernel has yet to write; the copies
+// after the wait read the coherent L2).
+__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap *map, int c0, int c1, int c2) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(c0), "r"(c1), "r"(c2)
+               : "memory");
+}
+__device__ __forceinline__ void tma_prefetch_4d(const CUtensorMap *map, int c0, int c1, int c2,
+                                                int c3) {
+  asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+               : "memory");
+}
+// Bytes of operand boxes a CTA prefetches into L2 before its grid dependency
+// wait (the first k-blocks of its first work unit): a few hundred KB a CTA
+// keeps the prefetches of a whole grid well inside L2.
+constexpr uint32_t kPrefetchBytes = 256 * 1024;
+
 // Bulk-tensor store of a shared-memory box (one thread), as its own group.
 __device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, uint32_t src, int c0, int c1,
                                              int c2) {
@@ -471,6 +493,26 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     prefetch_tmap(&tmA);
     prefetch_tmap(&tmB);
     if (p.c_tma) prefetch_tmap(&tmC);
+  }
+  if ((warp == 0 || warp == 6) && lane == 0 && (int)blockIdx.x < p.total_units) {
+    // the first k-blocks of this CTA's first unit into L2, A by warp 0, B by warp 6
+    int tm, tn, b, sp;
+    decode_unit(p, blockIdx.x, tm, tn, b, sp);
+    const int kb0 = sp * p.kb_per_split;
+    const int kb1 = min(min(p.num_kb, kb0 + p.kb_per_split), kb0 + (int)(kPrefetchBytes / STAGE_BYTES));
+    for (int kb = kb0; kb < kb1; ++kb) {
+      if (warp == 0) {
+        if (!p.a_mn) tma_prefetch_3d(&tmA, kb * BK, tm * BM, b);
+        else if (p.a_4d) tma_prefetch_4d(&tmA, 0, kb * BK, tm * (BM / ATOM), b);
+        else
+          for (int j = 0; j < p.a_boxes; ++j) tma_prefetch_3d(&tmA, tm * BM + j * ATOM, kb * BK, b);
+      } else {
+        if (!p.b_mn) tma_prefetch_3d(&tmB, kb * BK, tn * BN, b);
+        else if (p.b_4d) tma_prefetch_4d(&tmB, 0, kb * BK, tn * (BN / ATOM), b);
+        else
+          for (int j = 0; j < p.b_boxes; ++j) tma_prefetch_3d(&tmB, tn * BN + j * ATOM, kb * BK, b);
+      }
+    }
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
@@ -903,6 +945,29 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     prefetch_tmap(&tmA);
     prefetch_tmap(&tmB);
     prefetch_tmap(&tmBh);
+  }
+  if ((warp == 0 || warp == 6) && lane == 0 && cid < p.total_units) {
+    // the first k-blocks of this CTA's share of its first unit into L2
+    int tm, t0, b, w;
+    pair_unit(p, cid, CL * BN, tm, t0, b, w);
+    const int nw = w / CL, nh = nw / 2;
+    const int m0 = tm * PAIR_M + (int)pos * BM;
+    const int n0 = t0 + (int)pair * nw + (int)pos * nh;
+    const int kb1 = min(p.num_kb, (int)(kPrefetchBytes / STAGE_BYTES));
+    for (int kb = 0; kb < kb1; ++kb) {
+      if (warp == 0) {
+        if (!p.a_mn) tma_prefetch_3d(&tmA, kb * BK, m0, b);
+        else if (p.a_4d) tma_prefetch_4d(&tmA, 0, kb * BK, m0 / ATOM, b);
+        else
+          for (int j = 0; j < p.a_boxes; ++j) tma_prefetch_3d(&tmA, m0 + j * ATOM, kb * BK, b);
+      } else {
+        if (!p.b_mn) tma_prefetch_3d(&tmB, kb * BK, n0, b);  // box of BN/2 columns: covers this share
+        else if (p.b_4d && nh == BNH) tma_prefetch_4d(&tmB, 0, kb * BK, n0 / ATOM, b);
+        else
+          for (int j = 0; j < nh / ATOM; ++j)
+            tma_prefetch_3d(p.b_4d ? &tmBh : &tmB, n0 + j * ATOM, kb * BK, b);
+      }
+    }
   }
   if (warp == 1) {
     tmem_alloc_pair(smem_u32(tmem_slot), TMEM_COLS);
