@@ -153,6 +153,55 @@ def test_results_deterministic():
         assert np.array_equal(r1.view(np.uint8), c.result().view(np.uint8)), NAMES[i]
 
 
+def test_gemv_n_stream_interleaved_shapes():
+    """Shapes that change the number of column groups, splits and batch items
+    from call to call on one stream, which share one scratch buffer and one
+    set of arrival counters: every result must match the oracle."""
+    import torch
+    i = NAMES.index("gemv_n_stream")
+    cases = [Case(1, 4096, 4096, layout="NN", dist="int4", seed=21),
+             Case(1, 1000, 700, layout="NN", dist="int4", seed=22),
+             Case(1, 296, 900, layout="NN", dist="int4", seed=23, batch=3, pad=(8, 8, 4),
+                  bstride_extra=(8, 16, 8)),
+             Case(1, 8, 20000, layout="NN", dist="int4", seed=24)]
+    for k in [0, 1, 0, 2, 3, 0, 1, 2, 3, 3, 0]:
+        c = cases[k].device()
+        assert run(i, c) == mm.MM_OK, mm.mm_last_error()
+        c.check(exact=True)
+    s = torch.cuda.Stream()
+    c = cases[0].device()
+    assert mm.mm_execute_candidate(i, *c.args(), stream=s) == mm.MM_OK, mm.mm_last_error()
+    s.synchronize()
+    c.check(exact=True)
+
+
+def test_gemv_n_stream_graph_replay():
+    """A captured call replayed with new inputs each time: the arrival
+    counters live in device memory and are back at zero after every call,
+    so every replay must be exact."""
+    import torch
+    i = NAMES.index("gemv_n_stream")
+    c = Case(1, 4096, 4096, layout="NN", dist="int4", seed=30).device()
+    s = torch.cuda.Stream()
+    assert mm.mm_execute_candidate(i, *c.args(), stream=s) == mm.MM_OK, mm.mm_last_error()
+    s.synchronize()
+    c.check(exact=True)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        st = mm.mm_execute_candidate(i, *c.args(), stream=s)
+    assert st == mm.MM_OK, mm.mm_last_error()
+    for rep in range(3):
+        n = Case(1, 4096, 4096, layout="NN", dist="int4", seed=31 + rep)
+        for dst, op in ((c.dA, n.A), (c.dB, n.B), (c.dC, n.C)):
+            raw = op.buf.view(np.uint8)
+            dst[:raw.size].copy_(torch.from_numpy(raw.copy()))
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        n.dA, n.dB, n.dC = c.dA, c.dB, c.dC
+        n.check(exact=True)
+
+
 @pytest.mark.parametrize("shape_pad", [((1, 4096, 4096), 0), ((1, 1000, 700), 4), ((1, 5, 20000), 0),
                                        ((1, 70000, 24), 0), ((1, 300, 4100), 4), ((1, 77, 3), 5)],
                          ids=lambda s: "x".join(map(str, s[0])) + f"+{s[1]}")
