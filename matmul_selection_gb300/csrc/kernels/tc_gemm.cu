@@ -494,8 +494,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     prefetch_tmap(&tmB);
     if (p.c_tma) prefetch_tmap(&tmC);
   }
-  if ((warp == 0 || warp == 6) && lane == 0 && (int)blockIdx.x < p.total_units) {
-    // the first k-blocks of this CTA's first unit into L2, A by warp 0, B by warp 6
+  // the first k-blocks of this CTA's first unit into L2, A by warp 0, B by
+  // warp 6 (B only when it fills a box: a short B, such as the swapped form
+  // of a GEMV with a few rows, is small, shared by every CTA, and its
+  // mostly out-of-range boxes measured slower prefetched than not)
+  if ((warp == 0 || (warp == 6 && p.N >= BN)) && lane == 0 && (int)blockIdx.x < p.total_units) {
     int tm, tn, b, sp;
     decode_unit(p, blockIdx.x, tm, tn, b, sp);
     const int kb0 = sp * p.kb_per_split;
