@@ -747,15 +747,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 // the leader's "full" barrier (tx = both halves); the leader's commits are
 // multicast to the "empty" and "tmem full" barriers of both CTAs; both CTAs'
 // epilogue warps arrive on the leader's "tmem empty" barrier.  Each SM thus
-// loads half as many B bytes per k-block as the single-SM form.
-//
-// CL = 2 puts two pairs side by side along N in one cluster of four (ranks
-// 0-1: pair 0, ranks 2-3: pair 1).  Both pairs need the same 256 rows of A:
-// each CTA loads half of its 128 rows and multicasts them to the CTA at the
-// same position in the other pair, so each A byte leaves L2 once for 512
-// output columns.  A stage of a CTA is then written by both pairs' producers,
-// so its "empty" barrier waits for both pairs' MMAs (one commit from each
-// leader, multicast to all four CTAs).
+// loads half as many B bytes per k-block as the single-SM form.  Every CTA
+// loads its own operand tiles: no copy is multicast to another CTA.
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
@@ -792,19 +785,6 @@ __device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap
       "@e cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.cta_group::2"
       " [%0], [%1, {%3, %4, %5}], [%2];\n\t}" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(leader_bar), "r"(c0), "r"(c1), "r"(c2)
-      : "memory");
-}
-// The same copy delivered to every CTA in `mask` (same shared-memory offset in
-// each); each destination's bytes complete on the barrier at `leader_bar`'s
-// offset in the even CTA of that destination's pair.  Warp-collective.
-__device__ __forceinline__ void tma_load_3d_pair_mc(uint32_t dst, const CUtensorMap *map,
-                                                    uint32_t leader_bar, int c0, int c1, int c2,
-                                                    uint16_t mask) {
-  asm volatile(
-      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
-      "@e cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
-      ".multicast::cluster.cta_group::2 [%0], [%1, {%3, %4, %5}], [%2], %6;\n\t}" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(leader_bar), "r"(c0), "r"(c1), "r"(c2), "h"(mask)
       : "memory");
 }
 // Warp-collective.
@@ -894,7 +874,7 @@ __device__ __forceinline__ void pair_unit(const TcParams &p, int u, int bn, int 
   nw = half < 0 ? bn : bn / 2;
 }
 
-template <int BN, int STAGES, int ES, int CL>
+template <int BN, int STAGES, int ES>
 __global__ void __launch_bounds__(kTcThreads, 1)
     tc2_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                     const __grid_constant__ CUtensorMap tmB,
@@ -924,17 +904,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint32_t rank = cluster_ctarank();
-  const uint32_t pos = rank & 1u, pair = rank >> 1;  // position in the pair, pair in the cluster
+  const uint32_t pos = cluster_ctarank();  // position in the pair
   const bool leader = pos == 0;
-  const uint16_t pair_mask = (uint16_t)(0x3u << (2 * pair));
-  const uint16_t all_mask = (uint16_t)((1u << (2 * CL)) - 1u);
+  const uint16_t pair_mask = 0x3u;
   const int cid = (int)cluster_id_x(), ncl = (int)nclusters_x();
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full0 + 8 * s, 1);
-      mbar_init(empty0 + 8 * s, CL);  // one commit from each pair's leader
+      mbar_init(empty0 + 8 * s, 1);  // one commit from the leader
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull0 + 8 * a, 1);
@@ -952,10 +930,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if ((warp == 0 || warp == 6) && lane == 0 && cid < p.total_units) {
     // the first k-blocks of this CTA's share of its first unit into L2
     int tm, t0, b, w;
-    pair_unit(p, cid, CL * BN, tm, t0, b, w);
-    const int nw = w / CL, nh = nw / 2;
+    pair_unit(p, cid, BN, tm, t0, b, w);
+    const int nh = w / 2;
     const int m0 = tm * PAIR_M + (int)pos * BM;
-    const int n0 = t0 + (int)pair * nw + (int)pos * nh;
+    const int n0 = t0 + (int)pos * nh;
     const int kb1 = min(p.num_kb, (int)(kPrefetchBytes / STAGE_BYTES));
     for (int kb = 0; kb < kb1; ++kb) {
       if (warp == 0) {
@@ -980,8 +958,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   cluster_sync_all();  // barriers of both CTAs initialised before any remote use
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  const uint32_t leader_full0 = map_to_rank(full0, rank & ~1u);
-  const uint32_t leader_tempty0 = map_to_rank(tempty0, rank & ~1u);
+  const uint32_t leader_full0 = map_to_rank(full0, 0);
+  const uint32_t leader_tempty0 = map_to_rank(tempty0, 0);
   pdl_wait();  // the prologue above touched no global memory
 
   if (warp == 0 || warp == 6) {
@@ -997,11 +975,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       bool ok = true;
       for (int u = cid; u < p.total_units && ok; u += ncl) {
         int tm, t0, b, w;
-        pair_unit(p, u, CL * BN, tm, t0, b, w);
-        const int nw = w / CL;   // this pair's columns
-        const int nh = nw / 2;   // B columns this CTA loads for the unit
+        pair_unit(p, u, BN, tm, t0, b, w);
+        const int nh = w / 2;    // B columns this CTA loads for the unit
         const int m0 = tm * PAIR_M + (int)pos * BM;
-        const int n0 = t0 + (int)pair * nw + (int)pos * nh;
+        const int n0 = t0 + (int)pos * nh;
         const uint32_t tx = 2 * (A_BYTES + (uint32_t)nh * 128);
         for (int kb = 0; kb < p.num_kb; ++kb) {
           if (!warp_wait(empty0 + 8 * stage, phase ^ 1, abort_flag, p.err, kErrProducer,
@@ -1014,27 +991,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           const uint32_t sb = sa + A_BYTES;
           if (copy_a) {
             if (leader) mbar_expect_tx(full0 + 8 * stage, tx);
-            if constexpr (CL == 1) {
-              if (!p.a_mn) {
-                tma_load_3d_pair(sa, &tmA, lfb, kb * BK, m0, b);
-              } else if (p.a_4d) {
-                tma_load_4d_pair(sa, &tmA, lfb, 0, kb * BK, m0 / ATOM, b);
-              } else {
-                for (int j = 0; j < p.a_boxes; ++j)
-                  tma_load_3d_pair(sa + j * p.a_box_stride, &tmA, lfb, m0 + j * ATOM, kb * BK, b);
-              }
+            if (!p.a_mn) {
+              tma_load_3d_pair(sa, &tmA, lfb, kb * BK, m0, b);
+            } else if (p.a_4d) {
+              tma_load_4d_pair(sa, &tmA, lfb, 0, kb * BK, m0 / ATOM, b);
             } else {
-              // half of this CTA's A rows, to the same position in both pairs
-              const uint16_t amask = (uint16_t)(0x5u << pos);
-              if (!p.a_mn)  // box of BM / 2 rows
-                tma_load_3d_pair_mc(sa + pair * (BM / 2) * 128, &tmA, lfb, kb * BK,
-                                    m0 + (int)pair * (BM / 2), b, amask);
-              else          // one of the two 64-row boxes
-                tma_load_3d_pair_mc(sa + pair * p.a_box_stride, &tmA, lfb, m0 + (int)pair * ATOM,
-                                    kb * BK, b, amask);
+              for (int j = 0; j < p.a_boxes; ++j)
+                tma_load_3d_pair(sa + j * p.a_box_stride, &tmA, lfb, m0 + j * ATOM, kb * BK, b);
             }
           } else if (!p.b_mn) {
-            tma_load_3d_pair(sb, nw == BN ? &tmB : &tmBh, lfb, kb * BK, n0, b);
+            tma_load_3d_pair(sb, w == BN ? &tmB : &tmBh, lfb, kb * BK, n0, b);
           } else if (p.b_4d && nh == BNH) {
             tma_load_4d_pair(sb, &tmB, lfb, 0, kb * BK, n0 / ATOM, b);
           } else {  // with a 4-D map in tmB, tmBh holds the per-box 3-D map
@@ -1067,8 +1033,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       bool ok = true;
       for (int u = cid; u < p.total_units && ok; u += ncl) {
         int tm_, t0_, b_, w;
-        pair_unit(p, u, CL * BN, tm_, t0_, b_, w);
-        const uint32_t idesc = w == CL * BN ? p.idesc : p.idesc_half;
+        pair_unit(p, u, BN, tm_, t0_, b_, w);
+        const uint32_t idesc = w == BN ? p.idesc : p.idesc_half;
         if (!warp_wait(tempty0 + 8 * acc, acc_phase ^ 1, abort_flag, p.err, kErrMma,
                        p.timeout_ns))
           break;
@@ -1088,7 +1054,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           for (int kk = 0; kk < KSTEPS; ++kk)
             umma_pair<ES>(d_tmem, adesc + (uint64_t)(kk * p.a_kstep),
                           bdesc + (uint64_t)(kk * p.b_kstep), idesc, (kb > 0 || kk > 0) ? 1u : 0u);
-          umma_commit_multicast(empty0 + 8 * stage, all_mask);
+          umma_commit_multicast(empty0 + 8 * stage, pair_mask);
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1;
@@ -1112,8 +1078,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     uint32_t acc_phase = 0;
     for (int u = cid; u < p.total_units; u += ncl) {
       int tm, t0, b, w;
-      pair_unit(p, u, CL * BN, tm, t0, b, w);
-      const int nw = w / CL, n0 = t0 + (int)pair * nw;
+      pair_unit(p, u, BN, tm, t0, b, w);
+      const int nw = w, n0 = t0;
       if (!warp_wait(tfull0 + 8 * acc, acc_phase, abort_flag, p.err, kErrEpilogue, p.timeout_ns))
         break;
       tc_fence_after();
@@ -1138,16 +1104,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   tc_fence_before();
   __syncthreads();
   // After an abort, copies issued into stages that were never armed (B copies
-  // ahead of the arming, the other pair's multicasts) are not covered by the
-  // drain above: give any such copy time to land before shared memory is
-  // released.
+  // ahead of the arming) are not covered by the drain above: give any such
+  // copy time to land before shared memory is released.
   if (*abort_flag) {
     const uint64_t t0 = global_ns();
     while (global_ns() - t0 < 100000ull) __nanosleep(1000);
   }
-  // the leaders' MMAs (reading both CTAs' smem, writing both TMEMs) are done;
-  // with CL = 2 the other pair's copies into this CTA completed on our
-  // leader's barriers, which its producer drained
+  // the leader's MMAs (reading both CTAs' smem, writing both TMEMs) are done
   cluster_sync_all();
   tc_fence_after();
   if (warp == 1) tmem_dealloc_pair(tmem_base, TMEM_COLS);
@@ -1265,21 +1228,19 @@ struct TcCfg {
   int stages;
   bool splitk;
   bool pair;    // 2-SM (cta_group::2) kernel, tile M = 256
-  int cl;       // pairs per cluster (2: two pairs along N share A by multicast)
 };
 
 // In the tuner's priority order: where a round ends early (a candidate within
 // the roofline limit), the earlier entry wins, so the configurations that are
 // fastest on large problems come first.
 const TcCfg kCfgs[] = {
-    {"tc2_256x256_s7", 256, 7, false, true, 1},
-    {"tc2x2_256x256_s7", 256, 7, false, true, 2},
-    {"tc2_256x128_s8", 128, 8, false, true, 1},
-    {"tc_128x256_s4", 256, 4, false, false, 1},
-    {"tc_128x128_s6", 128, 6, false, false, 1},
-    {"tc_128x64_s8", 64, 8, false, false, 1},
-    {"tc_splitk_128x128_s6", 128, 6, true, false, 1},
-    {"tc_splitk_128x64_s8", 64, 8, true, false, 1},
+    {"tc2_256x256_s7", 256, 7, false, true},
+    {"tc2_256x128_s8", 128, 8, false, true},
+    {"tc_128x256_s4", 256, 4, false, false},
+    {"tc_128x128_s6", 128, 6, false, false},
+    {"tc_128x64_s8", 64, 8, false, false},
+    {"tc_splitk_128x128_s6", 128, 6, true, false},
+    {"tc_splitk_128x64_s8", 64, 8, true, false},
 };
 
 size_t smem_bytes(int bn, int stages) {
@@ -1380,12 +1341,12 @@ mm_status launch_kernel(const CUtensorMap &ma, const CUtensorMap &mb, const CUte
   return MM_OK;
 }
 
-template <int BN, int STAGES, int ES, int CL>
+template <int BN, int STAGES, int ES>
 struct PairKernel {
   static cudaLaunchConfig_t config(size_t smem, cudaStream_t s, cudaLaunchAttribute *attr) {
     cudaLaunchConfig_t lc = {};
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2 * CL;
+    attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     lc.blockDim = dim3(kTcThreads);
@@ -1396,7 +1357,7 @@ struct PairKernel {
     return lc;
   }
   static size_t smem() {
-    const TcCfg shape{"", BN, STAGES, false, true, CL};
+    const TcCfg shape{"", BN, STAGES, false, true};
     return smem_bytes_cfg(shape);
   }
   // Set-up once: shared-memory attribute and how many pairs fit at once.
@@ -1405,12 +1366,12 @@ struct PairKernel {
     static cudaError_t err = cudaSuccess;
     static int clusters = 0;
     std::call_once(once, [] {
-      auto kern = tc2_gemm_kernel<BN, STAGES, ES, CL>;
+      auto kern = tc2_gemm_kernel<BN, STAGES, ES>;
       err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem());
       if (err == cudaSuccess) {
         cudaLaunchAttribute attr[1];
         cudaLaunchConfig_t q = config(smem(), nullptr, attr);
-        q.gridDim = dim3(2 * CL);
+        q.gridDim = dim3(2);
         err = cudaOccupancyMaxActiveClusters(&clusters, kern, &q);
       }
     });
@@ -1421,9 +1382,8 @@ struct PairKernel {
   }
   static mm_status launch(const CUtensorMap &ma, const CUtensorMap &mb, const CUtensorMap &mbh,
                           const TcParams &tp, int clusters, cudaStream_t s) {
-    cudaError_t e = launch_pdl(tc2_gemm_kernel<BN, STAGES, ES, CL>,
-                               dim3((unsigned)(2 * CL * clusters)), dim3(kTcThreads), smem(), s,
-                               dim3(2 * CL), ma, mb, mbh, tp);
+    cudaError_t e = launch_pdl(tc2_gemm_kernel<BN, STAGES, ES>, dim3((unsigned)(2 * clusters)),
+                               dim3(kTcThreads), smem(), s, dim3(2), ma, mb, mbh, tp);
     if (e != cudaSuccess) return cuda_error(e, "tc2_gemm_kernel launch");
     return MM_OK;
   }
@@ -1431,18 +1391,16 @@ struct PairKernel {
 
 template <int ES>
 mm_status pair_capacity(int cfg, int *max_clusters) {
-  if (kCfgs[cfg].cl == 2) return PairKernel<256, 7, ES, 2>::capacity(max_clusters);
-  if (kCfgs[cfg].bn == 256) return PairKernel<256, 7, ES, 1>::capacity(max_clusters);
-  return PairKernel<128, 8, ES, 1>::capacity(max_clusters);
+  if (kCfgs[cfg].bn == 256) return PairKernel<256, 7, ES>::capacity(max_clusters);
+  return PairKernel<128, 8, ES>::capacity(max_clusters);
 }
 
 template <int ES>
 mm_status dispatch_pair(int cfg, const CUtensorMap &ma, const CUtensorMap &mb,
                         const CUtensorMap &mbh, const TcParams &tp, int clusters,
                         cudaStream_t s) {
-  if (kCfgs[cfg].cl == 2) return PairKernel<256, 7, ES, 2>::launch(ma, mb, mbh, tp, clusters, s);
-  if (kCfgs[cfg].bn == 256) return PairKernel<256, 7, ES, 1>::launch(ma, mb, mbh, tp, clusters, s);
-  return PairKernel<128, 8, ES, 1>::launch(ma, mb, mbh, tp, clusters, s);
+  if (kCfgs[cfg].bn == 256) return PairKernel<256, 7, ES>::launch(ma, mb, mbh, tp, clusters, s);
+  return PairKernel<128, 8, ES>::launch(ma, mb, mbh, tp, clusters, s);
 }
 
 template <int ES>
@@ -1693,14 +1651,11 @@ mm_status launch_tc_impl(const Problem &p, LaunchCtx &ctx, int cfg, bool c_trans
   const int bn = c.bn;
   const int bn_cta = c.pair ? bn / 2 : bn;  // B columns one CTA loads
   const int tile_m = c.pair ? 2 * BM : BM;
-  const int group_n = c.pair ? bn * c.cl : bn;  // columns of one work unit
   CUtensorMap ma, mb;
   mm_status st;
   // A: logical M x K.  K-major when stored row-major (N), MN-major when T.
-  // With two pairs per cluster each CTA loads half of its rows.
   if (!p.at)
-    st = encode_map(&ma, p.ta, p.A, p.K, p.M, p.batch, p.lda * es, p.sA * es, bk,
-                    c.cl == 2 ? BM / 2 : BM);
+    st = encode_map(&ma, p.ta, p.A, p.K, p.M, p.batch, p.lda * es, p.sA * es, bk, BM);
   else
     st = encode_map(&ma, p.ta, p.A, p.M, p.K, p.batch, p.lda * es, p.sA * es, atom, bk);
   if (st != MM_OK) return st;
@@ -1713,7 +1668,7 @@ mm_status launch_tc_impl(const Problem &p, LaunchCtx &ctx, int cfg, bool c_trans
   // MN-major operands: one 4-D copy per stage instead of one copy per
   // 128-byte-wide box, where the MN extent is a whole number of boxes
   const int a_nbox = BM / atom, b_nbox = bn_cta / atom;
-  const bool a_4d = p.at && c.cl == 1 && a_nbox > 1 && p.M % atom == 0;
+  const bool a_4d = p.at && a_nbox > 1 && p.M % atom == 0;
   const bool b_4d = !p.bt && b_nbox > 1 && p.N % atom == 0;
   const CUtensorMap mb3 = mb;  // per-box map (half-width units of the pair kernel)
   if (a_4d) {
@@ -1735,7 +1690,7 @@ mm_status launch_tc_impl(const Problem &p, LaunchCtx &ctx, int cfg, bool c_trans
   tp.K = (int)p.K;
   tp.batch = (int)p.batch;
   tp.tiles_m = (int)ceil_div(p.M, tile_m);
-  tp.tiles_n = (int)ceil_div(p.N, group_n);
+  tp.tiles_n = (int)ceil_div(p.N, bn);
   tp.num_kb = (int)ceil_div(p.K, bk);
   const int64_t tiles = (int64_t)tp.tiles_m * tp.tiles_n * tp.batch;
   if (c.splitk) {
