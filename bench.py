@@ -61,6 +61,7 @@ for _m in (1, 16, 127, 1000, 4097, 8192):
             _m, 4096, 4096, "N" + _t, (BF16, BF16, BF16), "normal", "normal", 4, 1, 1004)
 
 DEFAULT_WORKLOAD = "square_4096_bf16"
+GEMV_WORKLOAD = "gemv_m1_4096_bf16"
 
 
 def load_peaks():
@@ -92,6 +93,16 @@ def make_host_inputs(w):
                            dist=w["dist_b"])
     C = synth.output_buffer(w["dt"][2], M, N, batch=batch)
     return A, B, C
+
+
+def workload_config(w, name, n_gpus):
+    """The `config` object of a line: the same keys for both arms."""
+    return {"workload": name, "M": w["M"], "N": w["N"], "K": w["K"], "layout": w["layout"],
+            "batch": w["batch"],
+            "lda": (w["M"] if w["layout"][0] == "T" else w["K"]) + w["pad"],
+            "dtypes": [synth.DTYPE_NAMES[x] for x in w["dt"]],
+            "parallelism": f"replicas{n_gpus}",
+            "l2": "inputs rotate over sets totalling more than 2 x L2 between steps"}
 
 
 def algorithmic(w):
@@ -202,8 +213,7 @@ def run_reference(args, w, name):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": t / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "impl": "reference",
-        "config": {"workload": name, "M": M, "N": N, "K": K, "layout": w["layout"],
-                   "batch": batch},
+        "config": workload_config(w, name, args.gpus),
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                          "sample": f"{npts} random output elements per step (K={K} each)"},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
@@ -281,7 +291,10 @@ def traffic_for(kernel_name, workload):
     return e.get("dram_bytes_per_launch")
 
 
-def run_ours(args, w, name, rank, world, peaks, quiet=False):
+def run_ours(args, w, name, rank, world, peaks, lite=False):
+    """One workload through the library.  lite: only the cold tune, the warm
+    timed loop and the roofline (no cache-hit latency loop, no clock record,
+    no end-to-end leg), for a sub-record of the main line."""
     import torch
 
     import matmul_selection_gb300 as mm
@@ -343,7 +356,7 @@ def run_ours(args, w, name, rank, world, peaks, quiet=False):
         winner = mm.mm_candidate_name(mm.mm_lookup(st[1])[1])
         # warm cache-hit latency: host wall time of call + sync
         hits = []
-        for i in range(200 if args.report else 1000):
+        for i in range(100 if lite else 200 if args.report else 1000):
             t0 = time.perf_counter()
             call(i)
             torch.cuda.synchronize()
@@ -367,8 +380,9 @@ def run_ours(args, w, name, rank, world, peaks, quiet=False):
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
-    sampler.start()
-    time.sleep(0.3)
+    if not lite:
+        sampler.start()
+        time.sleep(0.3)
     launches0 = mm.mm_get_stats()["launches"]
     ev0.record(stream)
     for i in range(args.steps):
@@ -378,7 +392,20 @@ def run_ours(args, w, name, rank, world, peaks, quiet=False):
     launches = mm.mm_get_stats()["launches"] - launches0
     if world > 1:
         torch.distributed.barrier()
-    clocks = sampler.stop()
+    # the sampler polls every 200 ms and a timed region of a few steps is far
+    # shorter: keep the same workload running, untimed, for about half a
+    # second more so that the clock record reflects this load
+    t_hold = time.perf_counter()
+    i = 0
+    while not lite and time.perf_counter() - t_hold < 0.5:
+        for _ in range(50):
+            call(i)
+            i += 1
+        torch.cuda.synchronize()
+    clocks = None
+    if not lite:
+        clocks = sampler.stop()
+        clocks["window"] = "timed region plus 0.5 s of the same calls after it"
     total_ms = ev0.elapsed_time(ev1)
     # every warm step is one call of the tuned candidate: its mean device time
     # per launch is the timed loop's device time over the steps
@@ -405,23 +432,27 @@ def run_ours(args, w, name, rank, world, peaks, quiet=False):
         torch.cuda.synchronize()
         cublas_tflops = flops * nrep / (e0.elapsed_time(e1) * 1e-3) / 1e12
     # end to end from pinned host buffers through the host entry point
-    e2e_steps = max(1, min(args.steps, 50))
-    pA = torch.empty(A.buf.nbytes, dtype=torch.uint8, pin_memory=True)
-    pB = torch.empty(B.buf.nbytes, dtype=torch.uint8, pin_memory=True)
-    pC = torch.empty(C.buf.nbytes, dtype=torch.uint8, pin_memory=True)
-    pA.copy_(hA)
-    pB.copy_(hB)
-    mm.check(mm.mm_autotune_execute_host(pA.data_ptr(), pB.data_ptr(), pC.data_ptr(), M, N, K,
-                                         A.ld, B.ld, C.ld, dt, w["layout"], b, sh))
-    if world > 1:
-        torch.distributed.barrier()
-    t0 = time.perf_counter()
-    for _ in range(e2e_steps):
+    e2e = None
+    if not lite:
+        e2e_steps = max(1, min(args.steps, 50))
+        pA = torch.empty(A.buf.nbytes, dtype=torch.uint8, pin_memory=True)
+        pB = torch.empty(B.buf.nbytes, dtype=torch.uint8, pin_memory=True)
+        pC = torch.empty(C.buf.nbytes, dtype=torch.uint8, pin_memory=True)
+        pA.copy_(hA)
+        pB.copy_(hB)
         mm.check(mm.mm_autotune_execute_host(pA.data_ptr(), pB.data_ptr(), pC.data_ptr(), M, N,
                                              K, A.ld, B.ld, C.ld, dt, w["layout"], b, sh))
-    e2e_s = time.perf_counter() - t0
-    e2e_s = max_over_ranks(e2e_s, world, dev)
-    e2e_value = aggregate_rate(flops * e2e_steps, world, e2e_s) / 1e12
+        if world > 1:
+            torch.distributed.barrier()
+        t0 = time.perf_counter()
+        for _ in range(e2e_steps):
+            mm.check(mm.mm_autotune_execute_host(pA.data_ptr(), pB.data_ptr(), pC.data_ptr(), M,
+                                                 N, K, A.ld, B.ld, C.ld, dt, w["layout"], b, sh))
+        e2e_s = time.perf_counter() - t0
+        e2e_s = max_over_ranks(e2e_s, world, dev)
+        e2e = {"value": aggregate_rate(flops * e2e_steps, world, e2e_s) / 1e12, "unit": "TFLOP/s",
+               "steps": e2e_steps, "h2d_bytes_per_step": int(A.buf.nbytes + B.buf.nbytes),
+               "d2h_bytes_per_step": int(M * N * batch * synth.DTYPE_BYTES[dt[2]])}
     # roofline of the dominant (tuned) kernel: the bound is whichever of the
     # memory time (algorithmic bytes / HBM peak) and the compute time
     # (flops / tensor peak) is longer
@@ -448,17 +479,12 @@ def run_ours(args, w, name, rank, world, peaks, quiet=False):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": {BF16: "bf16", F16: "f16", F32: "f32"}[dt[0]], "data": "synthetic",
-        "config": {"workload": name, "M": M, "N": N, "K": K, "layout": w["layout"],
-                   "batch": batch, "lda": A.ld, "dtypes": [synth.DTYPE_NAMES[x] for x in dt],
-                   "parallelism": f"replicas{world}",
-                   "l2": f"{R} rotating input sets of {set_bytes / 1e6:.1f} MB (> 2 x L2)"},
+        "config": workload_config(w, name, world),
+        "rotation": f"{R} input sets of {set_bytes / 1e6:.1f} MB",
         "winner": winner, "cold_tune_ms": cold_ms, "cache_hit_ms": hit_ms,
         "host_enqueue_us": enqueue_us,
         "context_cublas_tflops": cublas_tflops,
-        "gpu_launches": int(launches), "clocks": clocks, "roofline": roof,
-        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "steps": e2e_steps,
-                "h2d_bytes_per_step": int(A.buf.nbytes + B.buf.nbytes),
-                "d2h_bytes_per_step": int(M * N * batch * synth.DTYPE_BYTES[dt[2]])},
+        "gpu_launches": int(launches), "clocks": clocks, "roofline": roof, "e2e": e2e,
     }
     if hbm:
         line["gbs"] = nbytes * args.steps * world / (total_ms * 1e-3) / 1e9
@@ -505,6 +531,21 @@ def main():
             args.steps = min(steps, 200)
         line, (A, B) = run_ours(args, wl, name, rank, world, peaks)
         args.steps = steps
+        if name == DEFAULT_WORKLOAD and not args.report and not args.candidate:
+            # the second target's workload, timed the same way, as a sub-record
+            args.steps = max(steps, 200)
+            g, _ = run_ours(args, workload_shape(GEMV_WORKLOAD), GEMV_WORKLOAD, rank, world, peaks,
+                            lite=True)
+            args.steps = steps
+            r = g["roofline"]
+            line["gemv_m1"] = {"workload": GEMV_WORKLOAD, "winner": g["winner"],
+                               "kernel_us": r["kernel_ms"] * 1e3, "value_gbs": r["achieved"],
+                               "frac": r["frac"], "peak_gbs": r["peak"], "bound": r["bound"],
+                               "steps": max(steps, 200),
+                               "cold_tune_ms": g["cold_tune_ms"],
+                               "cache_hit_ms": g["cache_hit_ms"],
+                               "gpu_launches": g["gpu_launches"],
+                               "traffic": r["traffic"]}
         if rank == 0:
             import oracle
             oracle.build()

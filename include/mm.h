@@ -150,9 +150,12 @@ mm_status mm_autotune_execute_host(const void *lhs, const void *rhs, void *out, 
  * device, a CSV in the format of TunableOp's result file (the guide's section
  * 3.2): "Validator,<NAME>,<value>" rows followed by
  * "MatmulKey,<key text>,<candidate name>,<median ms>,<all candidates>" rows.
- * Validators: MM_VERSION, CANDIDATE_CHECKSUM (hash of every candidate name
- * in registry order: renaming, adding or removing a candidate orphans old
- * entries, as on the autotune page's step 1), DEVICE, CUDA_VERSION.  Any
+ * Validators: MM_VERSION (the library version, the part of mm_version()
+ * before '+'), CANDIDATE_CHECKSUM (mm_candidate_checksum() as 16 hex digits:
+ * a hash of every candidate name in registry order, so renaming, adding or
+ * removing a candidate orphans old entries, as on the autotune page's step
+ * 1), DEVICE ("<device name>|sm_<major><minor>": the model, so a table tuned
+ * on one unit serves every unit of that model) and CUDA_VERSION (runtime).  Any
  * validator mismatch rejects the WHOLE file (MM_ERR_CACHE_VALIDATION).  A row
  * naming an unknown candidate is skipped; "Default" means the default kernel.
  *   path  NULL -> MM_CACHE_FILE; the device ordinal is inserted before the
@@ -187,6 +190,10 @@ int32_t mm_candidate_count(void);
 const char *mm_candidate_name(int32_t index); /* NULL if out of range */
 /* Launches of one candidate by this process (benchmark + execute). */
 uint64_t mm_candidate_launches(int32_t index);
+/* FNV-1a 64 hash of every candidate name (each followed by a newline) in
+ * registry order, then of the library version: the CANDIDATE_CHECKSUM
+ * validator of the result file.  Host only. */
+uint64_t mm_candidate_checksum(void);
 
 /*
  * mm_execute_candidate -- run one candidate directly (no key, no table):
@@ -236,7 +243,10 @@ double mm_roofline_limit_ns(double ops, double peak_ops_per_s, double bytes,
  *   numerical_check ("" or "atol_rtol"), cache_file (""), decisions
  *   ("" | "stdout" | path), verbose (0), peak_tflops (0 = probe/nominal),
  *   peak_gbs (0 = probe), fault ("" | "<candidate>:<mode>", host-side
- *   fault injection; modes error, nan, slow, wrong).
+ *   fault injection; modes error, nan, slow, wrong, stall: the host sleeps
+ *   1.5 s before benchmarking that candidate), record_untuned (""),
+ *   pending_wait_ms (120000: how long a miss on a key that another thread is
+ *   tuning waits before it runs the default kernel instead).
  * An environment variable, when set, takes precedence over the API (the
  * environment is read once, at first use).  Errors: MM_ERR_NOT_FOUND for an
  * unknown name, MM_ERR_INVALID_ARG for a bad value.
@@ -265,17 +275,36 @@ const char *mm_version(void);
  * `stream`.  The K-slice partial sums go to a fixed 16 MiB workspace that is
  * part of the library's device image (held on every GPU that loads the
  * library until exit): M*N must be at most 2,097,120 (two fp32 slices), else
- * MM_ERR_INVALID_ARG with the limit in the message.  The first call on a
- * device resolves the workspace's device address (cudaGetSymbolAddress) with
- * that device current; make it before any stream capture.  All calls share
- * the workspace, so calls whose GPU execution overlaps (two streams, two
- * threads) race and must be ordered by the caller.  Alignment and type rules
- * are those of the tensor-core candidates (16-byte aligned A, B and leading
- * dimensions; f32 only as NT), else MM_ERR_UNSUPPORTED.
+ * MM_ERR_INVALID_ARG with the limit in the message.  Differences from
+ * mm_autotune_execute for the same arguments: K = 0 is rejected
+ * (MM_ERR_INVALID_ARG) instead of writing zeros, and K must span at least two
+ * 128-byte blocks (K > 64 for bf16/f16, K > 32 for f32), else
+ * MM_ERR_UNSUPPORTED; alignment and type rules are those of the tensor-core
+ * candidates (16-byte aligned A, B and leading dimensions; f32 only as NT),
+ * else MM_ERR_UNSUPPORTED.
+ * The first call on a device resolves the workspace's device address
+ * (cudaGetSymbolAddress) with that device current; make it before any stream
+ * capture.  The address is kept for the life of the process, or until
+ * mm_shutdown, which forgets it (call mm_shutdown after a cudaDeviceReset).
+ * All calls share the workspace, so calls whose GPU execution overlaps (two
+ * streams, two threads) race and must be ordered by the caller.
+ * A kernel whose bounded wait gives up records a code in the workspace; the
+ * call itself has returned MM_OK by then (it is asynchronous) and its product
+ * is wrong.  mm_splitk_gemm_noalloc_status reports it.
  */
 mm_status mm_splitk_gemm_noalloc(const void *lhs, const void *rhs, void *out, int64_t M,
                                  int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
                                  mm_dtypes dt, mm_layout layout, void *stream);
+
+/*
+ * mm_splitk_gemm_noalloc_status -- synchronises `stream`, then reads the
+ * no-allocation workspace's error word on the current device (a 4-byte copy
+ * to the host; nothing is allocated).  MM_OK when no kernel of
+ * mm_splitk_gemm_noalloc gave up a bounded wait since the previous query;
+ * otherwise clears the word and returns MM_ERR_TIMEOUT (the products of those
+ * calls may be wrong).  Errors: MM_ERR_CUDA.
+ */
+mm_status mm_splitk_gemm_noalloc_status(void *stream);
 
 /* Free every library-owned device buffer and the tables; saves the table of
  * each device to MM_CACHE_FILE first when that option is set and tuning

@@ -82,6 +82,7 @@ _sig = {
     "mm_candidate_count": (_i32, []),
     "mm_candidate_name": (_cp, [_i32]),
     "mm_candidate_launches": (ctypes.c_uint64, [_i32]),
+    "mm_candidate_checksum": (ctypes.c_uint64, []),
     "mm_execute_candidate": (_i32, [_i32, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64, _i64,
                                     mm_dtypes, ctypes.c_int, ctypes.POINTER(mm_batch), _vp]),
     "mm_lookup": (_i32, [ctypes.POINTER(mm_key), _P32]),
@@ -98,6 +99,7 @@ _sig = {
     "mm_shutdown": (None, []),
     "mm_splitk_gemm_noalloc": (_i32, [_vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64, _i64,
                                       mm_dtypes, ctypes.c_int, _vp]),
+    "mm_splitk_gemm_noalloc_status": (_i32, [_vp]),
 }
 for _name, (_res, _args) in _sig.items():
     _f = getattr(_lib, _name)
@@ -227,6 +229,10 @@ def mm_candidate_launches(i):
     return _lib.mm_candidate_launches(i)
 
 
+def mm_candidate_checksum():
+    return _lib.mm_candidate_checksum()
+
+
 def candidate_names():
     return [mm_candidate_name(i) for i in range(mm_candidate_count())]
 
@@ -288,6 +294,12 @@ def mm_splitk_gemm_noalloc(lhs, rhs, out, M, N, K, lda, ldb, ldc, dtypes, layout
     """Split-K GEMM into the library's fixed workspace: no device allocation."""
     return _lib.mm_splitk_gemm_noalloc(_ptr(lhs), _ptr(rhs), _ptr(out), M, N, K, lda, ldb, ldc,
                                        _dt(dtypes), _layout(layout), _stream(stream))
+
+
+def mm_splitk_gemm_noalloc_status(stream=None):
+    """Synchronise `stream` and report (and clear) a bounded wait that gave up
+    in a no-allocation call since the previous query."""
+    return _lib.mm_splitk_gemm_noalloc_status(_stream(stream))
 
 
 def library_handle():

@@ -8,7 +8,10 @@
 // first, separated by ';' -- kept so an entry can be inspected after the fact
 // (burn "autotune" page, section "cache: in-memory table and default.db").
 // Validators (mismatch of any one rejects the WHOLE file, as TunableOp's
-// ValidateAll does): MM_VERSION, CANDIDATE_CHECKSUM, DEVICE, CUDA_VERSION.
+// ValidateAll does): MM_VERSION (the library version), CANDIDATE_CHECKSUM
+// (the candidate set), DEVICE (the device model and architecture, not one
+// unit: a table tuned on one GB300 serves every GB300, as TunableOp's result
+// file names the GPU architecture) and CUDA_VERSION (the runtime).
 // A row naming an unknown candidate is skipped; "Default" names the default
 // (naive) kernel, as TunableOp's hand-edit rule allows.
 #include <algorithm>
@@ -17,10 +20,6 @@
 #include <sstream>
 
 #include "common.h"
-
-#ifndef MM_BUILD_ID
-#define MM_BUILD_ID "dev"
-#endif
 
 namespace mm {
 
@@ -32,9 +31,8 @@ std::vector<std::pair<std::string, std::string>> validators(const DeviceState &d
   int rt = 0;
   cudaRuntimeGetVersion(&rt);
   char dev[256];
-  snprintf(dev, sizeof dev, "%s|sm_%d%d|%s", ds.info.name.c_str(), ds.info.cc_major,
-           ds.info.cc_minor, ds.info.uuid.c_str());
-  return {{"MM_VERSION", std::string(kVersion) + "+" + MM_BUILD_ID},
+  snprintf(dev, sizeof dev, "%s|sm_%d%d", ds.info.name.c_str(), ds.info.cc_major, ds.info.cc_minor);
+  return {{"MM_VERSION", kVersion},
           {"CANDIDATE_CHECKSUM", cks},
           {"DEVICE", dev},
           {"CUDA_VERSION", std::to_string(rt)}};

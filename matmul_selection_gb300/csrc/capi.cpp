@@ -160,6 +160,8 @@ const char *mm_candidate_name(int32_t index) {
 
 uint64_t mm_candidate_launches(int32_t index) { return candidate_launches(index); }
 
+uint64_t mm_candidate_checksum(void) { return registry_checksum(); }
+
 mm_status mm_execute_candidate(int32_t index, const void *lhs, const void *rhs, void *out,
                                int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
                                int64_t ldc, mm_dtypes dt, mm_layout layout, const mm_batch *batch,
@@ -274,6 +276,7 @@ void mm_shutdown(void) {
       if (ds.dirty) cache_save(ds, device_file_name(oo.cache_file, ds.info.ordinal));
     });
   release_all_devices();
+  noalloc_forget_devices();
 }
 
 }  // extern "C"

@@ -68,7 +68,7 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
 
 namespace mm {
 
-constexpr const char *kVersion = "0.1.0";
+constexpr const char *kVersion = "0.2.0";
 
 // ---------------------------------------------------------------- problem
 struct Problem {
@@ -166,9 +166,14 @@ struct Options {
   double peak_gbs = 0.0;
   std::string fault;
   std::string record_untuned;  // path: keys missed with tuning off are appended here
+  double pending_wait_ms = 120000.0;  // how long a miss waits for another thread's tuner
 };
-// Snapshot of the current options (env values take precedence over the API).
+// The current options (env values take precedence over the API), through a
+// per-thread copy refreshed when an option changes.
 const Options &get_options();
+// The same, built afresh under the options lock: for code that may run after
+// the calling thread's thread-local objects are gone (exit handlers).
+Options snapshot();
 mm_status set_option(const std::string &name, const std::string &value);
 mm_status get_option(const std::string &name, std::string *value);
 
@@ -235,6 +240,8 @@ struct DeviceState {
 mm_status current_device(DeviceState **out);
 // Drop every device state (mm_shutdown).
 void release_all_devices();
+// Forget the no-allocation entry point's per-device workspace addresses.
+void noalloc_forget_devices();
 void for_each_device(void (*fn)(DeviceState &));
 
 // Scratch of at least `bytes` private to (device, stream, slot).  A new or

@@ -640,7 +640,9 @@ void stream_plan(int64_t N, int64_t K, int64_t batch, int eb, int sms, int64_t *
 int mt_of(int64_t M) { return M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : 8; }
 
 constexpr int kMaxM = 8;
-constexpr size_t kMaxSmem = 96 * 1024;
+// shared memory of one CTA: instances that keep two CTAs an SM (MT <= 2)
+// stay within half of it; the others (one CTA an SM) may take most of it
+size_t max_smem(int mt) { return mt <= 2 ? 96 * 1024 : 200 * 1024; }
 
 size_t smem_n(int mt, int ks, int eb) {
   return ((size_t)ks * mt + (size_t)kWarps * mt * (256 / eb)) * sizeof(float);
@@ -766,7 +768,8 @@ bool gemv_fast_supports(const Problem &p, const DeviceInfo &d, int cfg, std::str
   } else {
     smem = c.b_trans ? smem_t(mt, p.K) : smem_n(mt, rows_per_rank(p.K), eb);
   }
-  if (smem > kMaxSmem || (int64_t)smem > d.smem_optin) return no("A slice too large for shared memory");
+  if (smem > max_smem(mt) || (int64_t)smem > d.smem_optin)
+    return no("A slice too large for shared memory");
   return true;
 }
 

@@ -11,19 +11,21 @@
 //
 // The workspace is a file-scope __device__ array of kScratchBytes (16 MiB),
 // present on every GPU that loads the library until the process exits.  It
-// holds the fp32 partial sums of the K slices (and, in its last 256 bytes,
-// the kernel's error word).  Host code cannot use the array's name as a
-// device address -- on the host it only names a stand-in object -- so the
-// device address is obtained once per device with cudaGetSymbolAddress and
-// cached.  That set-up happens on the first call on each device, with that
-// device current; make the first call before any stream capture.
+// holds the fp32 partial sums of the K slices and, in its last 256 bytes, the
+// kernels' error word.  Host code cannot use the array's name as a device
+// address -- on the host it only names a stand-in object -- so the device
+// address is obtained with cudaGetSymbolAddress, with the device current, on
+// the first call on each device, and kept until mm_shutdown (which forgets it,
+// so a call after a device reset resolves it again).  Make the first call on
+// a device before any stream capture.
 //
-// Every call shares the one array and it keeps the last call's contents:
-// the error word is cleared at the start of each call (the partials need no
-// clearing: each call overwrites every element it later reads).  Calls whose
-// GPU execution overlaps -- on two streams, or from two host threads --
-// race on the array and corrupt each other's results; the caller must order
-// them.
+// Every call shares the one array and it keeps the last call's contents.  The
+// partials need no clearing: each call overwrites every element it later
+// reads.  The error word starts at zero (static storage) and is cleared only
+// by mm_splitk_gemm_noalloc_status, so that query reports a bounded wait that
+// gave up in any call since the previous query.  Calls whose GPU execution
+// overlaps -- on two streams, or from two host threads -- race on the array
+// and corrupt each other's results; the caller must order them.
 #include <mutex>
 
 #include "../common.h"
@@ -42,43 +44,60 @@ namespace {
 constexpr int kMaxDevices = 64;
 
 struct StaticSetup {
-  std::once_flag once;
-  cudaError_t status = cudaSuccess;
+  bool ready = false;
   void *ptr = nullptr;
   DeviceInfo info;
 };
+std::mutex g_setup_mu;
 StaticSetup g_setup[kMaxDevices];
 
 // Resolve the array's device address and the device's properties, once per
-// device.  Queries only: nothing here allocates.
-mm_status setup_device(int dev, StaticSetup **out) {
+// device until forgotten.  Queries only: nothing here allocates.
+mm_status setup_device(int dev, StaticSetup *out) {
   if (dev < 0 || dev >= kMaxDevices) return set_error(MM_ERR_INVALID_ARG, "device ordinal %d", dev);
+  std::lock_guard<std::mutex> lk(g_setup_mu);
   StaticSetup &st = g_setup[dev];
-  std::call_once(st.once, [&] {
+  if (!st.ready) {
     void *p = nullptr;
     cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-    if (e == cudaSuccess) {
-      int sms = 0, maj = 0, min = 0, smem = 0;
-      e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-      if (e == cudaSuccess) e = cudaDeviceGetAttribute(&maj, cudaDevAttrComputeCapabilityMajor, dev);
-      if (e == cudaSuccess) e = cudaDeviceGetAttribute(&min, cudaDevAttrComputeCapabilityMinor, dev);
-      if (e == cudaSuccess)
-        e = cudaDeviceGetAttribute(&smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-      st.info.ordinal = dev;
-      st.info.sms = sms;
-      st.info.cc_major = maj;
-      st.info.cc_minor = min;
-      st.info.smem_optin = smem;
+    if (e != cudaSuccess) return cuda_error(e, "cudaGetSymbolAddress (static workspace)");
+    int v[4] = {0, 0, 0, 0};
+    const cudaDeviceAttr attrs[4] = {cudaDevAttrMultiProcessorCount, cudaDevAttrComputeCapabilityMajor,
+                                     cudaDevAttrComputeCapabilityMinor,
+                                     cudaDevAttrMaxSharedMemoryPerBlockOptin};
+    for (int i = 0; i < 4; ++i) {
+      e = cudaDeviceGetAttribute(&v[i], attrs[i], dev);
+      if (e != cudaSuccess) return cuda_error(e, "cudaDeviceGetAttribute");
     }
-    st.status = e;
+    st.info.ordinal = dev;
+    st.info.sms = v[0];
+    st.info.cc_major = v[1];
+    st.info.cc_minor = v[2];
+    st.info.smem_optin = v[3];
     st.ptr = p;
-  });
-  if (st.status != cudaSuccess) return cuda_error(st.status, "cudaGetSymbolAddress (static workspace)");
-  *out = &st;
+    st.ready = true;
+  }
+  *out = st;
   return MM_OK;
 }
 
+mm_status current_setup(StaticSetup *out) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_error(e, "cudaGetDevice");
+  return setup_device(dev, out);
+}
+
+int *error_word(const StaticSetup &su) {
+  return reinterpret_cast<int *>(static_cast<char *>(su.ptr) + kScratchBytes - kErrBytes);
+}
+
 }  // namespace
+
+void noalloc_forget_devices() {
+  std::lock_guard<std::mutex> lk(g_setup_mu);
+  for (auto &st : g_setup) st = StaticSetup();
+}
 
 }  // namespace mm
 
@@ -100,18 +119,31 @@ extern "C" mm_status mm_splitk_gemm_noalloc(const void *lhs, const void *rhs, vo
                      "holds %zu bytes (M*N <= %zu)",
                      (long long)M, (long long)N, need2, kScratchBytes - kErrBytes,
                      (kScratchBytes - kErrBytes) / (2 * sizeof(float)));
-  int dev = -1;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return cuda_error(e, "cudaGetDevice");
-  StaticSetup *su = nullptr;
-  if ((st = setup_device(dev, &su)) != MM_OK) return st;
+  StaticSetup su;
+  if ((st = current_setup(&su)) != MM_OK) return st;
   const int cfg = tc_config_index("tc_splitk_128x128_s6");
   if (cfg < 0) return set_error(MM_ERR_UNSUPPORTED, "split-K configuration missing");
+  return launch_tc_splitk_into(p, su.info, cfg, static_cast<float *>(su.ptr),
+                               kScratchBytes - kErrBytes, error_word(su),
+                               static_cast<cudaStream_t>(stream));
+}
+
+extern "C" mm_status mm_splitk_gemm_noalloc_status(void *stream) {
+  StaticSetup su;
+  mm_status st = current_setup(&su);
+  if (st != MM_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  char *base = static_cast<char *>(su->ptr);
-  int *err = reinterpret_cast<int *>(base + kScratchBytes - kErrBytes);
-  e = cudaMemsetAsync(err, 0, sizeof(int), s);
-  if (e != cudaSuccess) return cuda_error(e, "cudaMemsetAsync (error word)");
-  return launch_tc_splitk_into(p, su->info, cfg, reinterpret_cast<float *>(base),
-                               kScratchBytes - kErrBytes, err, s);
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_error(e, "cudaStreamSynchronize");
+  int code = 0;
+  e = cudaMemcpy(&code, error_word(su), sizeof code, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_error(e, "cudaMemcpy (error word)");
+  if (code == 0) return MM_OK;
+  const int zero = 0;
+  e = cudaMemcpy(error_word(su), &zero, sizeof zero, cudaMemcpyHostToDevice);
+  if (e != cudaSuccess) return cuda_error(e, "cudaMemcpy (clear error word)");
+  return set_error(MM_ERR_TIMEOUT,
+                   "a split-K kernel's bounded wait gave up (code 0x%x); the products of the "
+                   "calls since the previous status query may be wrong",
+                   code);
 }

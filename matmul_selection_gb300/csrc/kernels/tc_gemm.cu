@@ -446,6 +446,16 @@ __device__ __forceinline__ void decode_unit(const TcParams &p, int u, int &tm, i
   b = u / p.tiles_m;
 }
 
+// K blocks of a work unit.  Without split-K a unit takes every K block in
+// order.  With S = splits > 1, split sp takes the blocks sp, sp + S,
+// sp + 2S, ...: at any moment the S CTAs of a tile read S neighbouring K
+// blocks, so together they stream each operand row from one place (a run of
+// S * 128 bytes of every A row, say) instead of from S places far apart.
+__device__ __forceinline__ int unit_kblocks(const TcParams &p, int sp) {
+  return (p.num_kb - sp + p.splits - 1) / p.splits;
+}
+__device__ __forceinline__ int unit_kb(const TcParams &p, int sp, int i) { return sp + i * p.splits; }
+
 // ---------------------------------------------------------------- the kernel
 template <int BN, int STAGES, int ES>
 __global__ void __launch_bounds__(kTcThreads, 1)
@@ -501,9 +511,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if ((warp == 0 || (warp == 6 && p.N >= BN)) && lane == 0 && (int)blockIdx.x < p.total_units) {
     int tm, tn, b, sp;
     decode_unit(p, blockIdx.x, tm, tn, b, sp);
-    const int kb0 = sp * p.kb_per_split;
-    const int kb1 = min(min(p.num_kb, kb0 + p.kb_per_split), kb0 + (int)(kPrefetchBytes / STAGE_BYTES));
-    for (int kb = kb0; kb < kb1; ++kb) {
+    const int nk = min(unit_kblocks(p, sp), (int)(kPrefetchBytes / STAGE_BYTES));
+    for (int i = 0; i < nk; ++i) {
+      const int kb = unit_kb(p, sp, i);
       if (warp == 0) {
         if (!p.a_mn) tma_prefetch_3d(&tmA, kb * BK, tm * BM, b);
         else if (p.a_4d) tma_prefetch_4d(&tmA, 0, kb * BK, tm * (BM / ATOM), b);
@@ -539,9 +549,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       for (int u = blockIdx.x; u < p.total_units && ok; u += gridDim.x) {
         int tm, tn, b, sp;
         decode_unit(p, u, tm, tn, b, sp);
-        const int kb0 = sp * p.kb_per_split;
-        const int kb1 = min(p.num_kb, kb0 + p.kb_per_split);
-        for (int kb = kb0; kb < kb1; ++kb) {
+        const int nk = unit_kblocks(p, sp);
+        for (int i = 0; i < nk; ++i) {
+          const int kb = unit_kb(p, sp, i);
           if (!warp_wait(empty0 + 8 * stage, phase ^ 1, abort_flag, p.err, kErrProducer,
                          p.timeout_ns)) {
             ok = false;
@@ -604,9 +614,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
-        const int kb0 = sp * p.kb_per_split;
-        const int kb1 = min(p.num_kb, kb0 + p.kb_per_split);
-        for (int kb = kb0; kb < kb1; ++kb) {
+        const int nk = unit_kblocks(p, sp);
+        for (int i = 0; i < nk; ++i) {
           if (!warp_wait(full0 + 8 * stage, phase, abort_flag, p.err, kErrMma, p.timeout_ns)) {
             ok = false;
             break;
@@ -619,7 +628,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
           for (int kk = 0; kk < KSTEPS; ++kk)
             umma<ES>(d_tmem, adesc + (uint64_t)(kk * p.a_kstep), bdesc + (uint64_t)(kk * p.b_kstep),
-                     p.idesc, (kb > kb0 || kk > 0) ? 1u : 0u);
+                     p.idesc, (i > 0 || kk > 0) ? 1u : 0u);
           umma_commit(empty0 + 8 * stage);  // frees the stage when these MMAs finish
           if (++stage == STAGES) {
             stage = 0;

@@ -21,7 +21,7 @@ const OptDef kDefs[] = {{"tuning"},          {"autotune_cache"},
                         {"cache_file"},      {"decisions"},
                         {"verbose"},         {"peak_tflops"},
                         {"peak_gbs"},        {"fault"},
-                        {"record_untuned"}};
+                        {"record_untuned"},  {"pending_wait_ms"}};
 
 std::mutex g_mu;
 Options g_api;
@@ -96,6 +96,7 @@ bool apply(Options &o, const std::string &n, const std::string &v) {
   if (n == "peak_gbs") return parse_double(v, &o.peak_gbs);
   if (n == "fault") { o.fault = v; return true; }
   if (n == "record_untuned") { o.record_untuned = v; return true; }
+  if (n == "pending_wait_ms") return parse_double(v, &o.pending_wait_ms) && o.pending_wait_ms >= 0;
   return false;
 }
 
@@ -119,6 +120,7 @@ std::string show(const Options &o, const std::string &n) {
   if (n == "peak_gbs") { snprintf(b, sizeof b, "%g", o.peak_gbs); return b; }
   if (n == "fault") return o.fault;
   if (n == "record_untuned") return o.record_untuned;
+  if (n == "pending_wait_ms") { snprintf(b, sizeof b, "%g", o.pending_wait_ms); return b; }
   return "";
 }
 

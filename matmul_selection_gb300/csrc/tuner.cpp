@@ -36,6 +36,7 @@
 #include <cmath>
 #include <cstdio>
 #include <fstream>
+#include <thread>
 
 #include "common.h"
 
@@ -260,6 +261,8 @@ CandResult bench_candidate(int idx, BenchEnv &env, double best_ms) {
     return r;
   }
   bool faulty = env.fault.name == reg[idx].name;
+  if (faulty && env.fault.mode == "stall")  // a slow host-side benchmark (tests the pending wait)
+    std::this_thread::sleep_for(std::chrono::milliseconds(1500));
   int n = 0;
   double total = 0;
   int in_limit = 0;
@@ -364,12 +367,16 @@ std::string fin_json(const CandResult &r) {
 }
 
 void log_decision(const Options &o, const KeyPod &key, const std::vector<CandResult> &res,
-                  int winner, double limit_ms, const Peaks &pk, double ops, double bytes) {
+                  int winner, double limit_ms, const Peaks &pk, double ops, double bytes,
+                  int rotating_sets, bool l2_flush) {
   if (o.decisions.empty()) return;
   std::string s = "{\"key\": \"" + key_text(key) + "\", \"fastest_index\": " +
                   std::to_string(winner) + ", \"fastest\": \"" +
                   (winner >= 0 ? registry()[winner].name : std::string("")) + "\"";
   char b[512];
+  snprintf(b, sizeof b, ", \"rotating_sets\": %d, \"l2_flush\": %s", rotating_sets,
+           l2_flush ? "true" : "false");
+  s += b;
   snprintf(b, sizeof b,
            ", \"bounds\": {\"compute\": {\"amount\": %.0f, \"peak_per_s\": %.6g}, \"memory\": "
            "{\"amount\": %.0f, \"peak_per_s\": %.6g}, \"threshold\": 0.8, \"launch_overhead_ns\": "
@@ -419,6 +426,8 @@ mm_status tune(DeviceState &ds, const Problem &p, const KeyPod &key, const Optio
 
   std::vector<CandResult> res(registry().size());
   int winner = -1;
+  int rotating_sets = 0;
+  bool flushed = false;
   if (plan.size() == 1) {
     // a single candidate is recorded without measuring it (the page's step 2)
     winner = plan[0].cand;
@@ -436,10 +445,12 @@ mm_status tune(DeviceState &ds, const Problem &p, const KeyPod &key, const Optio
     env.fault = parse_fault(o.fault);
     env.limit_ms = limit_ms;
     env.ev.resize(20);
+    rotating_sets = (int)rot.sets.size();
     for (auto &e : env.ev) MM_CUDA_TRY(cudaEventCreate(&e));
     if (o.l2_flush) {
       st = ds.flush_buf.ensure((size_t)std::max<int64_t>(2 * ds.info.l2_bytes, 64 << 20));
       if (st != MM_OK) return st;
+      flushed = true;
     }
     std::vector<void *> extra;
     if (!o.numerical_check.empty()) {
@@ -530,7 +541,7 @@ mm_status tune(DeviceState &ds, const Problem &p, const KeyPod &key, const Optio
     cudaStreamSynchronize(ds.tune_stream);
     for (void *x : extra) cudaFree(x);
   }
-  log_decision(o, key, res, winner, limit_ms, pk, ops, bytes);
+  log_decision(o, key, res, winner, limit_ms, pk, ops, bytes, rotating_sets, flushed);
   if (winner < 0) {
     std::string why;
     for (const auto &r : res)
@@ -603,11 +614,14 @@ mm_status launch_default(DeviceState &ds, const KeyPod &key, const Problem &p, L
   return launch_candidate(0, p, ctx);
 }
 
+// Runs from exit(): the main thread's thread-local objects (get_options's
+// per-thread copy among them) are already destroyed, so the options are read
+// through a fresh snapshot.
 void save_at_exit_fn() {
-  Options o = get_options();
+  const Options o = snapshot();
   if (o.cache_file.empty() || !o.autotune_cache) return;
   for_each_device([](DeviceState &ds) {
-    Options oo = get_options();
+    const Options oo = snapshot();
     if (ds.dirty) cache_save(ds, device_file_name(oo.cache_file, ds.info.ordinal));
   });
 }
@@ -637,7 +651,8 @@ mm_status tune_and_record(DeviceState &ds, const Problem &p, const KeyPod &key, 
       }
     }
     if (ds.pending.count(key)) {
-      ds.pending_cv.wait_for(pl, std::chrono::seconds(120), [&] { return !ds.pending.count(key); });
+      ds.pending_cv.wait_for(pl, std::chrono::duration<double, std::milli>(o.pending_wait_ms),
+                             [&] { return !ds.pending.count(key); });
       pl.unlock();
       std::shared_lock<std::shared_mutex> lk(ds.table_mu);
       auto it = ds.table.find(key);

@@ -31,7 +31,7 @@ def test_every_declared_symbol_is_exported():
 
 
 def test_version_and_registry():
-    assert mm.mm_version().startswith("0.1.0+")
+    assert mm.mm_version().startswith("0.2.0+")
     names = mm.candidate_names()
     assert names[0] == "naive"
     assert len(names) == len(set(names))

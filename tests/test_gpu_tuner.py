@@ -20,7 +20,7 @@ NAMES = mm.candidate_names()
 DEFAULTS = {"tuning": "1", "autotune_cache": "1", "fault": "", "numerical_check": "",
             "decisions": "", "cache_file": "", "max_tuning_iterations": "100",
             "max_tuning_duration_ms": "30", "l2_flush": "0", "rotating_buffer_mb": "-1",
-            "record_untuned": ""}
+            "record_untuned": "", "pending_wait_ms": "120000"}
 
 
 @pytest.fixture(autouse=True)
@@ -390,3 +390,127 @@ def test_graph_capture_miss_uses_default():
     c.check(exact=True)
     assert mm.mm_get_stats()["tunes"] == 0
     assert mm.mm_candidate_launches(0) == n0 + 1
+
+
+# ---------------------------------------------------------------- harness paths
+def _last_decision(path):
+    return json.loads(open(path).read().splitlines()[-1])
+
+
+def test_l2_flush_times_every_call(tmp_path):
+    """With the L2 flush on, a flush kernel runs before every timed call, so
+    each call is timed on its own (one sample per call) and the finalists are
+    not re-timed; the tuned result is still the product."""
+    path = str(tmp_path / "flush.jsonl")
+    mm.check(mm.mm_set_option("l2_flush", "1"))
+    mm.check(mm.mm_set_option("decisions", path))
+    c = Case(256, 256, 256, dist="int4").device()
+    mm.check(execute(c))
+    c.check(exact=True)
+    rec = _last_decision(path)
+    assert rec["l2_flush"] is True
+    ok = [x for x in rec["candidates"] if x["state"] == "ok"]
+    assert ok and all(x["samples"] == x["n"] for x in ok), ok
+    assert not any("final_ms" in x for x in rec["candidates"])
+    for _ in range(3):  # warm calls
+        mm.check(execute(c))
+    c.check(exact=True)
+
+
+@pytest.mark.parametrize("mb,expect", [("0", 1), ("-1", None)])
+def test_rotating_buffer_size(tmp_path, mb, expect):
+    """rotating_buffer_mb = 0 turns the rotation off (one private output, the
+    caller's inputs read in place); the default (-1) rotates over enough sets
+    to cover twice the L2.  Either way the caller's output is only written by
+    the final launch and holds the product."""
+    path = str(tmp_path / "rot.jsonl")
+    mm.check(mm.mm_set_option("rotating_buffer_mb", mb))
+    mm.check(mm.mm_set_option("decisions", path))
+    c = Case(1, 4096, 4096, dt=(BF16, BF16, F32), dist="int4").device()
+    mm.check(execute(c))
+    c.check(exact=True)
+    rec = _last_decision(path)
+    if expect is not None:
+        assert rec["rotating_sets"] == expect
+    else:
+        import torch
+        l2 = torch.cuda.get_device_properties(0).L2_cache_size
+        set_bytes = (4096 + 4096 * 4096) * 2 + 4096 * 4
+        assert rec["rotating_sets"] * set_bytes >= 2 * l2
+
+
+def test_shutdown_saves_table_and_library_is_usable_again(tmp_path):
+    """mm_shutdown with a cache file set writes the device's table (file name
+    with the device ordinal) and frees the library's state; the next call on
+    the same key loads that file lazily and runs the recorded kernel without
+    tuning."""
+    base = str(tmp_path / "table.csv")
+    mm.check(mm.mm_set_option("cache_file", base))
+    c = Case(200, 136, 512, dist="int4", seed=9).device()
+    mm.check(execute(c))
+    c.check(exact=True)
+    tunes = mm.mm_get_stats()["tunes"]
+    assert tunes == 1
+    mm.mm_shutdown()
+    saved = str(tmp_path / "table0.csv")
+    assert os.path.exists(saved)
+    assert sum(l.startswith("MatmulKey,") for l in open(saved)) == 1
+    c.device()
+    mm.check(execute(c))
+    c.check(exact=True)
+    assert mm.mm_get_stats()["tunes"] == tunes, "the saved entry was not used"
+    assert mm.mm_cache_size() == 1
+
+
+def test_cache_file_loaded_lazily_on_first_miss(tmp_path):
+    """A table saved earlier is read when the first miss of a fresh library
+    state meets the cache_file option: both keys become hits, no tuning."""
+    ca = Case(64, 64, 64, dist="int4").device()
+    cb = Case(1, 512, 512, layout="NT", dist="int4").device()
+    mm.check(execute(ca))
+    mm.check(execute(cb))
+    mm.check(mm.mm_cache_save(str(tmp_path / "lazy0.csv")))
+    mm.mm_shutdown()
+    mm.mm_reset_stats()
+    mm.check(mm.mm_set_option("cache_file", str(tmp_path / "lazy.csv")))
+    for c in (ca, cb):
+        c.device()
+        mm.check(execute(c))
+        c.check(exact=True)
+    s = mm.mm_get_stats()
+    assert s["tunes"] == 0 and mm.mm_cache_size() == 2
+    assert s["hits"] == 1  # the second key found the table already loaded
+
+
+def test_pending_key_wait_runs_out_and_default_runs():
+    """A second caller missing on a key that another thread is still tuning
+    waits pending_wait_ms, then runs the default candidate instead of
+    waiting for the tuner; both results are the product and the key is tuned
+    once."""
+    import time
+    import torch
+    mm.check(mm.mm_set_option("fault", "gemv_n:stall"))  # the tuner sleeps 1.5 s on the host
+    mm.check(mm.mm_set_option("pending_wait_ms", "100"))
+    c1 = Case(1, 512, 512, dist="int4", seed=3).device()
+    c2 = Case(1, 512, 512, dist="int4", seed=4).device()
+    errs = []
+
+    def tuner():
+        torch.cuda.set_device(0)
+        st = mm.mm_autotune_execute(*c1.args())
+        if st != 0:
+            errs.append(mm.mm_last_error())
+
+    t = threading.Thread(target=tuner)
+    t.start()
+    time.sleep(0.4)  # the tuner holds the key (it sleeps inside its first benchmark)
+    t0 = time.perf_counter()
+    mm.check(execute(c2))
+    waited = time.perf_counter() - t0
+    c2.check(exact=True)
+    still_tuning = t.is_alive()
+    t.join()
+    assert not errs, errs
+    c1.check(exact=True)
+    assert still_tuning and waited < 1.0, (still_tuning, waited)
+    assert mm.mm_get_stats()["tunes"] == 1
