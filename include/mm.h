@@ -246,7 +246,13 @@ double mm_roofline_limit_ns(double ops, double peak_ops_per_s, double bytes,
  *   fault injection; modes error, nan, slow, wrong, stall: the host sleeps
  *   1.5 s before benchmarking that candidate), record_untuned (""),
  *   pending_wait_ms (120000: how long a miss on a key that another thread is
- *   tuning waits before it runs the default kernel instead).
+ *   tuning waits before it runs the default kernel instead), wait_limit_us
+ *   (2000000: how long a wait of a 1-SM tensor-core kernel's main loop may
+ *   last before the kernel gives up, records MM_ERR_TIMEOUT's cause in its
+ *   error word and returns; its drain waits keep 2 s), wait_stall (0; test
+ *   hook: 1 makes the MMA warp of those kernels first wait on a barrier that
+ *   nothing arrives on, so that the wait limit runs out and the kernel's
+ *   abort path runs; it never faults or hangs the device).
  * An environment variable, when set, takes precedence over the API (the
  * environment is read once, at first use).  Errors: MM_ERR_NOT_FOUND for an
  * unknown name, MM_ERR_INVALID_ARG for a bad value.
@@ -274,7 +280,8 @@ const char *mm_version(void);
  * out are device pointers the caller owns; the call is asynchronous on
  * `stream`.  The K-slice partial sums go to a fixed 16 MiB workspace that is
  * part of the library's device image (held on every GPU that loads the
- * library until exit): M*N must be at most 2,097,120 (two fp32 slices), else
+ * library until exit; its last 256 bytes hold an error word): M*N must be
+ * at most 2,097,120 (two fp32 slices), else
  * MM_ERR_INVALID_ARG with the limit in the message.  Differences from
  * mm_autotune_execute for the same arguments: K = 0 is rejected
  * (MM_ERR_INVALID_ARG) instead of writing zeros, and K must span at least two

@@ -167,6 +167,8 @@ struct Options {
   std::string fault;
   std::string record_untuned;  // path: keys missed with tuning off are appended here
   double pending_wait_ms = 120000.0;  // how long a miss waits for another thread's tuner
+  double wait_limit_us = 2000000.0;   // 1-SM tensor-core kernels: main-loop wait limit
+  int wait_stall = 0;                 // test hook: 1-SM kernels wait on a barrier nothing arrives on
 };
 // The current options (env values take precedence over the API), through a
 // per-thread copy refreshed when an option changes.

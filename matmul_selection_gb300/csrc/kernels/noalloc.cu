@@ -33,6 +33,7 @@
 namespace {
 constexpr size_t kScratchBytes = 16u << 20;
 constexpr size_t kErrBytes = 256;  // error word area at the end
+constexpr size_t kPartialBytes = kScratchBytes - kErrBytes;
 }  // namespace
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
@@ -89,7 +90,7 @@ mm_status current_setup(StaticSetup *out) {
 }
 
 int *error_word(const StaticSetup &su) {
-  return reinterpret_cast<int *>(static_cast<char *>(su.ptr) + kScratchBytes - kErrBytes);
+  return reinterpret_cast<int *>(static_cast<char *>(su.ptr) + kPartialBytes);
 }
 
 }  // namespace
@@ -113,19 +114,18 @@ extern "C" mm_status mm_splitk_gemm_noalloc(const void *lhs, const void *rhs, vo
   if (M == 0 || N == 0) return MM_OK;
   if (K == 0) return set_error(MM_ERR_INVALID_ARG, "K must be >= 1 (nothing to split)");
   const size_t need2 = 2 * (size_t)M * (size_t)N * sizeof(float);
-  if (need2 > kScratchBytes - kErrBytes)
+  if (need2 > kPartialBytes)
     return set_error(MM_ERR_INVALID_ARG,
                      "M x N = %lld x %lld needs %zu bytes for two K slices; the fixed workspace "
                      "holds %zu bytes (M*N <= %zu)",
-                     (long long)M, (long long)N, need2, kScratchBytes - kErrBytes,
-                     (kScratchBytes - kErrBytes) / (2 * sizeof(float)));
+                     (long long)M, (long long)N, need2, kPartialBytes,
+                     kPartialBytes / (2 * sizeof(float)));
   StaticSetup su;
   if ((st = current_setup(&su)) != MM_OK) return st;
-  const int cfg = tc_config_index("tc_splitk_128x128_s6");
+  const int cfg = tc_config_index("tc_splitk_128x128_s7");
   if (cfg < 0) return set_error(MM_ERR_UNSUPPORTED, "split-K configuration missing");
-  return launch_tc_splitk_into(p, su.info, cfg, static_cast<float *>(su.ptr),
-                               kScratchBytes - kErrBytes, error_word(su),
-                               static_cast<cudaStream_t>(stream));
+  return launch_tc_splitk_into(p, su.info, cfg, static_cast<float *>(su.ptr), kPartialBytes,
+                               error_word(su), static_cast<cudaStream_t>(stream));
 }
 
 extern "C" mm_status mm_splitk_gemm_noalloc_status(void *stream) {
@@ -139,9 +139,8 @@ extern "C" mm_status mm_splitk_gemm_noalloc_status(void *stream) {
   e = cudaMemcpy(&code, error_word(su), sizeof code, cudaMemcpyDeviceToHost);
   if (e != cudaSuccess) return cuda_error(e, "cudaMemcpy (error word)");
   if (code == 0) return MM_OK;
-  const int zero = 0;
-  e = cudaMemcpy(error_word(su), &zero, sizeof zero, cudaMemcpyHostToDevice);
-  if (e != cudaSuccess) return cuda_error(e, "cudaMemcpy (clear error word)");
+  e = cudaMemset(error_word(su), 0, sizeof(int));
+  if (e != cudaSuccess) return cuda_error(e, "cudaMemset (clear the error word)");
   return set_error(MM_ERR_TIMEOUT,
                    "a split-K kernel's bounded wait gave up (code 0x%x); the products of the "
                    "calls since the previous status query may be wrong",

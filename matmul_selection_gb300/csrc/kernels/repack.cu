@@ -69,7 +69,7 @@ const RepackCfg kRepackCfgs[] = {
     {"tc2_repack_256x256", "tc2_256x256_s7", false},
     {"tc_repack_128x128", "tc_128x128_s6", false},
     {"tc_repack_128x64", "tc_128x64_s8", false},
-    {"tc_repack_splitk_128x128", "tc_splitk_128x128_s6", false},
+    {"tc_repack_splitk_128x128", "tc_splitk_128x128_s7", false},
     {"tc_repack_splitk_128x64", "tc_splitk_128x64_s8", false},
     {"gemv_swap_tc_repack_splitk_128x64", "tc_splitk_128x64_s8", true},
 };

@@ -22,10 +22,10 @@
 //     multiplied as tf32: the burn backend page notes the kernel may run f32
 //     as tf32), fp32 accumulation always;
 //   * split-K configurations write fp32 partials of each K slice to a
-//     workspace; a second kernel adds the slices in a fixed order (runs of
-//     consecutive slices, each in increasing order, then the runs in order;
-//     deterministic) and converts.  Split-K regroups additions only (the
-//     CMU 15-779 lecture's rfactor / split-K discussion);
+//     workspace, one CTA a (tile, K slice); a second kernel adds the slices
+//     in a fixed order (runs of consecutive slices, each in increasing order,
+//     then the runs in order; deterministic) and converts.  Split-K regroups
+//     additions only (the CMU 15-779 lecture's rfactor / split-K discussion);
 //   * every mbarrier wait is bounded (%globaltimer); on expiry the kernel
 //     records an error code, tells the other roles to stop, waits for its own
 //     MMAs, frees TMEM and returns.
@@ -50,10 +50,12 @@ constexpr int kTcThreads = 224;
 // store path's [32][33] transpose scratch), then the barriers
 constexpr uint32_t kEpiStageBytes = 4 * 2 * 4096;
 constexpr uint32_t kBarBytes = 256;
-constexpr uint64_t kWaitTimeoutNs = 2000000000ull;  // 2 s per wait
+constexpr uint64_t kWaitTimeoutNs = 2000000000ull;   // 2 s per wait (main loops, default)
+constexpr uint64_t kDrainTimeoutNs = 2000000000ull;  // 2 s per drain wait, always
 
 // error codes (first one wins): 0x100 | role
-constexpr int kErrProducer = 0x101, kErrMma = 0x102, kErrEpilogue = 0x103, kErrDrain = 0x104;
+constexpr int kErrProducer = 0x101, kErrMma = 0x102, kErrEpilogue = 0x103, kErrDrain = 0x104,
+              kErrReduce = 0x105;
 
 struct TcParams {
   int M, N, K, batch;
@@ -75,6 +77,9 @@ struct TcParams {
   // output stored transposed: element (i, j) of the computed product goes to
   // C[j * ldc + i] (the swapped form C^T = B^T A^T of a product with small M)
   int c_trans;
+  // test hook: the MMA warp first waits on a barrier nothing arrives on, so
+  // that the wait limit runs out and the kernel's abort path runs
+  int stall_wait;
   // 1-SM kernel: C written by TMA bulk-tensor stores (tmC valid); with
   // splits > 1, tmC maps the fp32 workspace as [splits * batch][M][N]
   int c_tma;
@@ -169,6 +174,15 @@ __device__ __noinline__ void wait_drain(uint32_t bar, uint32_t parity, int *err,
       return;
     }
   }
+}
+
+// Lower the barrier's pending transaction count by `bytes` as if they had
+// arrived (for copies that were counted but never issued).  Warp-collective.
+__device__ __forceinline__ void mbar_complete_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e mbarrier.complete_tx.shared::cta.b64 [%0], %1;\n\t}" ::"r"(bar), "r"(bytes)
+      : "memory");
 }
 
 // Warp-collective.
@@ -446,18 +460,23 @@ __device__ __forceinline__ void decode_unit(const TcParams &p, int u, int &tm, i
   b = u / p.tiles_m;
 }
 
-// K blocks of a work unit.  Without split-K a unit takes every K block in
-// order.  With S = splits > 1, split sp takes the blocks sp, sp + S,
-// sp + 2S, ...: at any moment the S CTAs of a tile read S neighbouring K
-// blocks, so together they stream each operand row from one place (a run of
-// S * 128 bytes of every A row, say) instead of from S places far apart.
+// K blocks of a work unit: split sp takes the contiguous blocks
+// [sp * kb_per_split, (sp + 1) * kb_per_split) (all of them without split-K).
 __device__ __forceinline__ int unit_kblocks(const TcParams &p, int sp) {
-  return (p.num_kb - sp + p.splits - 1) / p.splits;
+  return min(p.kb_per_split, p.num_kb - sp * p.kb_per_split);
 }
-__device__ __forceinline__ int unit_kb(const TcParams &p, int sp, int i) { return sp + i * p.splits; }
+__device__ __forceinline__ int unit_kb(const TcParams &p, int sp, int i) {
+  return sp * p.kb_per_split + i;
+}
+
 
 // ---------------------------------------------------------------- the kernel
-template <int BN, int STAGES, int ES>
+// SK: a split-K configuration.  Each of its CTAs takes exactly one work unit
+// (the grid has one CTA a unit), so once the unit's MMAs are done the operand
+// ring is idle: the epilogue stages its stores in the ring, and the CTA needs
+// no shared memory beyond it (the ring can be a stage deeper) and one TMEM
+// accumulator.
+template <int BN, int STAGES, int ES, bool SK>
 __global__ void __launch_bounds__(kTcThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, const TcParams p) {
@@ -468,23 +487,29 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   constexpr int BK = 128 / ES;      // K elements per stage (one 128-byte swizzle row)
   constexpr int UMMA_K = 32 / ES;   // K per tcgen05.mma (32 bytes)
   constexpr int KSTEPS = BK / UMMA_K;
-  constexpr uint32_t TMEM_COLS = 2 * BN;
+  constexpr uint32_t TMEM_COLS = SK ? BN : 2 * BN;
   constexpr int ATOM = 128 / ES;    // elements per 128-byte row (MN-major box width)
+  static_assert(!SK || STAGES * STAGE_BYTES >= kEpiStageBytes + 2048,
+                "split-K epilogue staging and reduction scratch live in the ring");
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
-  uint8_t *epi_stage = smem + STAGES * STAGE_BYTES;  // 1024-byte aligned
-  uint64_t *bars = reinterpret_cast<uint64_t *>(epi_stage + kEpiStageBytes);
+  uint8_t *epi_stage = SK ? smem : smem + STAGES * STAGE_BYTES;  // 1024-byte aligned
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + STAGES * STAGE_BYTES + (SK ? 0 : kEpiStageBytes));
   const uint32_t full0 = smem_u32(bars);
   const uint32_t empty0 = full0 + 8 * STAGES;
   const uint32_t tfull0 = empty0 + 8 * STAGES;
   const uint32_t tempty0 = tfull0 + 16;
   const uint32_t drain = tempty0 + 16;
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * STAGES + 5);
+  const uint32_t stall = drain + 8;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * STAGES + 6);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // a split-K CTA takes its one unit (the host launches one CTA a unit); a
+  // persistent CTA walks the units with the grid stride
+  const int ustep = SK ? p.total_units : (int)gridDim.x;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -496,6 +521,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mbar_init(tempty0 + 8 * a, 4);  // one arrival per epilogue warp
     }
     mbar_init(drain, 1);
+    mbar_init(stall, 1);  // nothing ever arrives on it
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -546,7 +572,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      for (int u = blockIdx.x; u < p.total_units && ok; u += gridDim.x) {
+      int nfill = 0;  // stage fills this warp issued
+      for (int u = blockIdx.x; u < p.total_units && ok; u += ustep) {
         int tm, tn, b, sp;
         decode_unit(p, u, tm, tn, b, sp);
         const int nk = unit_kblocks(p, sp);
@@ -557,6 +584,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             ok = false;
             break;
           }
+          ++nfill;
           const uint32_t fb = full0 + 8 * stage;
           const uint32_t sa = smem_u32(smem + stage * STAGE_BYTES);
           const uint32_t sb = sa + A_BYTES;
@@ -584,16 +612,26 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
         }
       }
-      // Leave no copy in flight: wait until the MMA warp has released every
-      // stage we filled (normal path), or at least until our last fills
-      // landed (abort path).
+      // Leave no copy in flight.  Fill f of the ring is phase f / STAGES of
+      // stage f % STAGES's full barrier.  Without an abort both warps issue
+      // the same fills.  After an abort one warp may have issued up to a
+      // ring's worth more (it passed an empty barrier the other gave up on
+      // just before it completed): once both have stopped, warp 0 arms the
+      // stages that received B without an arming, and takes the B bytes that
+      // were counted but never issued off the stages it armed, so that every
+      // issued copy, and only those, completes its phase; then it waits for
+      // the last phase of every stage filled.
+      volatile int *fills = reinterpret_cast<volatile int *>(tmem_slot + 3);
+      if (lane == 0) fills[copy_a ? 0 : 1] = nfill;
+      asm volatile("bar.sync 2, 64;" ::: "memory");  // warps 0 and 6
       if (copy_a) {
-        for (int s = 0; s < STAGES; ++s) {
-          // the most recent fill of `stage` (walking backwards) used parity:
-          int st = (stage + s) % STAGES;
-          uint32_t par = (st < stage) ? phase : phase ^ 1;  // last completed-or-pending fill
-          wait_drain(full0 + 8 * st, par, p.err, kErrProducer, p.timeout_ns);
-        }
+        const int nb = fills[1];
+        for (int f = nfill; f < nb; ++f) mbar_expect_tx(full0 + 8 * (f % STAGES), B_BYTES);
+        for (int f = nb; f < nfill; ++f) mbar_complete_tx(full0 + 8 * (f % STAGES), B_BYTES);
+        const int total = max(nfill, nb);
+        for (int f = max(0, total - STAGES); f < total; ++f)
+          wait_drain(full0 + 8 * (f % STAGES), (uint32_t)(f / STAGES) & 1u, p.err, kErrProducer,
+                     kDrainTimeoutNs);
       }
     }
     __syncwarp();
@@ -604,8 +642,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       uint32_t phase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
-      bool ok = true;
-      for (int u = blockIdx.x; u < p.total_units && ok; u += gridDim.x) {
+      // (test hook: a wait that only its limit ends)
+      bool ok = !p.stall_wait || warp_wait(stall, 0, abort_flag, p.err, kErrMma, p.timeout_ns);
+      for (int u = blockIdx.x; u < p.total_units && ok; u += ustep) {
         int tm, tn, b, sp;
         decode_unit(p, u, tm, tn, b, sp);
 
@@ -644,7 +683,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       // every MMA this thread issued is complete before TMEM is released
       umma_commit(drain);
-      wait_drain(drain, 0, p.err, kErrDrain, p.timeout_ns);
+      wait_drain(drain, 0, p.err, kErrDrain, kDrainTimeoutNs);
     }
     __syncwarp();
   } else {
@@ -655,7 +694,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     int sbuf = 0;
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int u = blockIdx.x; u < p.total_units; u += gridDim.x) {
+    for (int u = blockIdx.x; u < p.total_units; u += ustep) {
       int tm, tn, b, sp;
       decode_unit(p, u, tm, tn, b, sp);
       if (!warp_wait(tfull0 + 8 * acc, acc_phase, abort_flag, p.err, kErrEpilogue, p.timeout_ns))
@@ -1028,7 +1067,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         for (int s = 0; s < STAGES; ++s) {
           int st = (stage + s) % STAGES;
           uint32_t par = (st < stage) ? phase : phase ^ 1;
-          wait_drain(full0 + 8 * st, par, p.err, kErrProducer, p.timeout_ns);
+          wait_drain(full0 + 8 * st, par, p.err, kErrProducer, kDrainTimeoutNs);
         }
     }
     __syncwarp();
@@ -1077,7 +1116,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
       }
       umma_commit_pair_local(drain);
-      wait_drain(drain, 0, p.err, kErrDrain, p.timeout_ns);
+      wait_drain(drain, 0, p.err, kErrDrain, kDrainTimeoutNs);
     }
     __syncwarp();
   } else {
@@ -1248,16 +1287,18 @@ const TcCfg kCfgs[] = {
     {"tc_128x256_s4", 256, 4, false, false},
     {"tc_128x128_s6", 128, 6, false, false},
     {"tc_128x64_s8", 64, 8, false, false},
-    {"tc_splitk_128x128_s6", 128, 6, true, false},
+    {"tc_splitk_128x128_s7", 128, 7, true, false},
     {"tc_splitk_128x64_s8", 64, 8, true, false},
 };
 
-size_t smem_bytes(int bn, int stages) {
-  return (size_t)stages * (BM * 128 + bn * 128) + 1024 + kEpiStageBytes + kBarBytes;
+// 1-SM kernel: the ring, the epilogue staging (split-K configurations stage
+// in the ring instead), the barriers and 1 KB of alignment slack.
+size_t smem_bytes(int bn, int stages, bool sk) {
+  return (size_t)stages * (BM * 128 + bn * 128) + 1024 + (sk ? 0 : kEpiStageBytes) + kBarBytes;
 }
 
 size_t smem_bytes_cfg(const TcCfg &c) {
-  if (!c.pair) return smem_bytes(c.bn, c.stages);
+  if (!c.pair) return smem_bytes(c.bn, c.stages, c.splitk);
   return (size_t)c.stages * (BM * 128 + (c.bn / 2) * 128) + kPairSlack + 1024 + 256;
 }
 
@@ -1333,19 +1374,18 @@ uint64_t smem_desc_bits(uint32_t lbo_bytes, uint32_t sbo_bytes) {
   return d;
 }
 
-template <int BN, int STAGES, int ES>
+template <int BN, int STAGES, int ES, bool SK>
 mm_status launch_kernel(const CUtensorMap &ma, const CUtensorMap &mb, const CUtensorMap &mc,
                         const TcParams &tp, int grid, cudaStream_t s) {
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
-  const size_t smem = smem_bytes(BN, STAGES);
+  const size_t smem = smem_bytes(BN, STAGES, SK);
+  auto kern = tc_gemm_kernel<BN, STAGES, ES, SK>;
   std::call_once(once, [&] {
-    attr_err = cudaFuncSetAttribute(tc_gemm_kernel<BN, STAGES, ES>,
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   });
   if (attr_err != cudaSuccess) return cuda_error(attr_err, "cudaFuncSetAttribute (tc smem)");
-  cudaError_t e = launch_pdl(tc_gemm_kernel<BN, STAGES, ES>, dim3(grid), dim3(kTcThreads), smem, s,
-                             dim3(1), ma, mb, mc, tp);
+  cudaError_t e = launch_pdl(kern, dim3(grid), dim3(kTcThreads), smem, s, dim3(1), ma, mb, mc, tp);
   if (e != cudaSuccess) return cuda_error(e, "tc_gemm_kernel launch");
   return MM_OK;
 }
@@ -1415,14 +1455,26 @@ mm_status dispatch_pair(int cfg, const CUtensorMap &ma, const CUtensorMap &mb,
 template <int ES>
 mm_status dispatch(int cfg, const CUtensorMap &ma, const CUtensorMap &mb, const CUtensorMap &mc,
                    const TcParams &tp, int grid, cudaStream_t s) {
+  const bool sk = kCfgs[cfg].splitk;
   switch (kCfgs[cfg].bn) {
-  case 256: return launch_kernel<256, 4, ES>(ma, mb, mc, tp, grid, s);
-  case 128: return launch_kernel<128, 6, ES>(ma, mb, mc, tp, grid, s);
-  default: return launch_kernel<64, 8, ES>(ma, mb, mc, tp, grid, s);
+  case 256: return launch_kernel<256, 4, ES, false>(ma, mb, mc, tp, grid, s);
+  case 128:
+    return sk ? launch_kernel<128, 7, ES, true>(ma, mb, mc, tp, grid, s)
+              : launch_kernel<128, 6, ES, false>(ma, mb, mc, tp, grid, s);
+  default:
+    return sk ? launch_kernel<64, 8, ES, true>(ma, mb, mc, tp, grid, s)
+              : launch_kernel<64, 8, ES, false>(ma, mb, mc, tp, grid, s);
   }
 }
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// The main-loop wait limit of the 1-SM kernels (option wait_limit_us; the
+// drain waits keep 2 s, and the 2-SM kernel keeps 2 s throughout).
+uint64_t one_sm_wait_limit_ns() {
+  const double us = get_options().wait_limit_us;
+  return us >= 0 ? (uint64_t)(us * 1000.0) : kWaitTimeoutNs;
+}
 
 // Split-K reduction plan: V = 4 outputs a thread when the workspace allows
 // 16-byte loads, else 1; G threads a group of V outputs (a power of two
@@ -1484,6 +1536,23 @@ void choose_splits(int64_t tiles, int64_t num_kb, int sms, int *splits, int *kb_
   int64_t per = ceil_div(num_kb, s);
   *kb_per = (int)per;
   *splits = (int)ceil_div(num_kb, per);
+}
+
+// Split-K (every CTA one unit): fp32 partials to tp.ws by bulk-tensor stores
+// where TMA can describe the workspace, then the reduction kernel, which
+// spreads the sums over every SM.  (Adding the partials inside the GEMM's
+// grid instead -- by the CTA that finishes a tile's last slice, or by all of
+// a tile's CTAs after waiting for one another -- measured slower on every
+// split-K shape: the CTAs it keeps resident hold back the next call's CTAs.)
+template <int ES>
+mm_status run_splitk(const Problem &p, TcParams &tp, int cfg, const CUtensorMap &ma,
+                     const CUtensorMap &mb, int sms, int c_trans, cudaStream_t s) {
+  CUtensorMap mw = ma;
+  mm_status st = ws_map(&mw, tp);
+  if (st != MM_OK) return st;
+  st = dispatch<ES>(cfg, ma, mb, mw, tp, tp.total_units, s);
+  if (st != MM_OK) return st;
+  return launch_reduce(tp, sms, p, c_trans, s);
 }
 
 }  // namespace
@@ -1548,7 +1617,8 @@ mm_status launch_tc_splitk_into(const Problem &p, const DeviceInfo &di, int cfg,
   tp.c_vec_ok = ((uintptr_t)p.C % 16 == 0) && ((p.ldc * ec) % 16 == 0) &&
                 (p.batch <= 1 || (p.sC * ec) % 16 == 0);
   tp.err = err;
-  tp.timeout_ns = kWaitTimeoutNs;
+  tp.timeout_ns = one_sm_wait_limit_ns();
+  tp.stall_wait = get_options().wait_stall;
   tp.a_mn = p.at ? 1 : 0;
   tp.b_mn = p.bt ? 0 : 1;
   const uint32_t fmt = p.ta == MM_F16 ? 0u : p.ta == MM_BF16 ? 1u : 2u;
@@ -1564,13 +1634,8 @@ mm_status launch_tc_splitk_into(const Problem &p, const DeviceInfo &di, int cfg,
   tp.a_box_stride = mn_atom_bytes;
   tp.b_box_stride = mn_atom_bytes;
   tp.ws = ws;
-  const int grid = (int)std::min<int64_t>(units, di.sms);
-  CUtensorMap mw = ma;
-  st = ws_map(&mw, tp);
-  if (st != MM_OK) return st;
-  st = es == 2 ? dispatch<2>(cfg, ma, mb, mw, tp, grid, s) : dispatch<4>(cfg, ma, mb, mw, tp, grid, s);
-  if (st != MM_OK) return st;
-  return launch_reduce(tp, di.sms, p, 0, s);
+  return es == 2 ? run_splitk<2>(p, tp, cfg, ma, mb, di.sms, 0, s)
+                 : run_splitk<4>(p, tp, cfg, ma, mb, di.sms, 0, s);
 }
 
 int tc_config_index(const char *name) {
@@ -1732,7 +1797,8 @@ mm_status launch_tc_impl(const Problem &p, LaunchCtx &ctx, int cfg, bool c_trans
   tp.c_vec_ok = ((uintptr_t)p.C % 16 == 0) && ((p.ldc * ec) % 16 == 0) &&
                 (p.batch <= 1 || (p.sC * ec) % 16 == 0);
   tp.err = ctx.dev->d_err;
-  tp.timeout_ns = kWaitTimeoutNs;
+  tp.timeout_ns = c.pair ? kWaitTimeoutNs : one_sm_wait_limit_ns();
+  tp.stall_wait = c.pair ? 0 : get_options().wait_stall;
   tp.a_mn = p.at ? 1 : 0;
   tp.b_mn = p.bt ? 0 : 1;
   const uint32_t fmt = p.ta == MM_F16 ? 0u : p.ta == MM_BF16 ? 1u : 2u;
@@ -1766,32 +1832,28 @@ mm_status launch_tc_impl(const Problem &p, LaunchCtx &ctx, int cfg, bool c_trans
     return es == 2 ? dispatch_pair<2>(cfg, ma, mb, mbh, tp, clusters, ctx.stream)
                    : dispatch_pair<4>(cfg, ma, mb, mbh, tp, clusters, ctx.stream);
   }
-  if (tp.splits > 1) {
+  const int sms = ctx.dev->info.sms;
+  if (c.splitk) {
     void *w = nullptr;
     size_t ws_bytes = (size_t)tp.splits * tp.batch * (size_t)p.M * p.N * sizeof(float);
     st = get_scratch(*ctx.dev, ctx.stream, SCRATCH_WORKSPACE, ws_bytes, &w);
     if (st != MM_OK) return st;
     tp.ws = static_cast<float *>(w);
+    return es == 2 ? run_splitk<2>(p, tp, cfg, ma, mb, sms, tp.c_trans, ctx.stream)
+                   : run_splitk<4>(p, tp, cfg, ma, mb, sms, tp.c_trans, ctx.stream);
   }
-  const int grid = (int)std::min<int64_t>(units, ctx.dev->info.sms);
-  // C (or the split-K workspace) by bulk-tensor stores where TMA can describe
-  // it, else the per-thread path
+  const int grid = (int)std::min<int64_t>(units, sms);
+  // C by bulk-tensor stores where TMA can describe it, else the per-thread path
   CUtensorMap mc = ma;
-  if (tp.splits > 1) {
-    st = ws_map(&mc, tp);
-    if (st != MM_OK) return st;
-  } else if (!c_trans && (uintptr_t)p.C % 16 == 0 && (p.ldc * ec) % 16 == 0 &&
+  if (!c_trans && (uintptr_t)p.C % 16 == 0 && (p.ldc * ec) % 16 == 0 &&
              (p.batch <= 1 || (p.sC * ec) % 16 == 0) && p.ldc * ec < (1LL << 40) &&
              p.sC * ec < (1LL << 40)) {
     st = encode_map(&mc, p.tc, p.C, p.N, p.M, p.batch, p.ldc * ec, p.sC * ec, 128 / ec, 32);
     if (st != MM_OK) return st;
     tp.c_tma = 1;
   }
-  st = es == 2 ? dispatch<2>(cfg, ma, mb, mc, tp, grid, ctx.stream)
-               : dispatch<4>(cfg, ma, mb, mc, tp, grid, ctx.stream);
-  if (st != MM_OK) return st;
-  if (tp.splits > 1) return launch_reduce(tp, ctx.dev->info.sms, p, tp.c_trans, ctx.stream);
-  return MM_OK;
+  return es == 2 ? dispatch<2>(cfg, ma, mb, mc, tp, grid, ctx.stream)
+                 : dispatch<4>(cfg, ma, mb, mc, tp, grid, ctx.stream);
 }
 
 }  // namespace

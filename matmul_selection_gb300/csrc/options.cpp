@@ -21,7 +21,8 @@ const OptDef kDefs[] = {{"tuning"},          {"autotune_cache"},
                         {"cache_file"},      {"decisions"},
                         {"verbose"},         {"peak_tflops"},
                         {"peak_gbs"},        {"fault"},
-                        {"record_untuned"},  {"pending_wait_ms"}};
+                        {"record_untuned"},  {"pending_wait_ms"},
+                        {"wait_limit_us"},   {"wait_stall"}};
 
 std::mutex g_mu;
 Options g_api;
@@ -97,6 +98,8 @@ bool apply(Options &o, const std::string &n, const std::string &v) {
   if (n == "fault") { o.fault = v; return true; }
   if (n == "record_untuned") { o.record_untuned = v; return true; }
   if (n == "pending_wait_ms") return parse_double(v, &o.pending_wait_ms) && o.pending_wait_ms >= 0;
+  if (n == "wait_limit_us") return parse_double(v, &o.wait_limit_us) && o.wait_limit_us >= 0;
+  if (n == "wait_stall") return parse_int(v, &o.wait_stall);
   return false;
 }
 
@@ -121,6 +124,8 @@ std::string show(const Options &o, const std::string &n) {
   if (n == "fault") return o.fault;
   if (n == "record_untuned") return o.record_untuned;
   if (n == "pending_wait_ms") { snprintf(b, sizeof b, "%g", o.pending_wait_ms); return b; }
+  if (n == "wait_limit_us") { snprintf(b, sizeof b, "%g", o.wait_limit_us); return b; }
+  if (n == "wait_stall") return std::to_string(o.wait_stall);
   return "";
 }
 

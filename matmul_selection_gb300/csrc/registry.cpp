@@ -14,8 +14,8 @@
 //   gemv   : MAX when the anchored m <= 16, else NEVER;
 //   tensor : HIGH; inside it plain tile configs are HIGH, split-K configs are
 //            HIGH when the output has too few tiles to fill the GPU and k is
-//            deep (anchored tiles*2 <= SMs and k >= 4*max(m, n) and k >= 1024),
-//            else MIN (backup);
+//            deep (anchored 128 x 128 tiles * 2 <= SMs and k >= 1024), else
+//            MIN (backup);
 //   naive  : MIN.
 #include <algorithm>
 

@@ -20,7 +20,8 @@ NAMES = mm.candidate_names()
 DEFAULTS = {"tuning": "1", "autotune_cache": "1", "fault": "", "numerical_check": "",
             "decisions": "", "cache_file": "", "max_tuning_iterations": "100",
             "max_tuning_duration_ms": "30", "l2_flush": "0", "rotating_buffer_mb": "-1",
-            "record_untuned": "", "pending_wait_ms": "120000"}
+            "record_untuned": "", "pending_wait_ms": "120000", "wait_limit_us": "2000000",
+            "wait_stall": "0"}
 
 
 @pytest.fixture(autouse=True)
@@ -514,3 +515,55 @@ def test_pending_key_wait_runs_out_and_default_runs():
     c1.check(exact=True)
     assert still_tuning and waited < 1.0, (still_tuning, waited)
     assert mm.mm_get_stats()["tunes"] == 1
+
+
+def test_wait_limit_timeout_is_reported(tmp_path):
+    """A 1-SM tensor-core kernel whose wait runs out (the test hook makes its
+    MMA warp first wait on a barrier nothing arrives on, limit 1 ms) records
+    a code in its error word, stops its other roles, lets its copies land
+    and returns.  The tuner marks those candidates `timeout` and picks
+    another; the no-allocation split-K call reports MM_ERR_TIMEOUT through its
+    status query.  Without the hook both give the exact product again."""
+    one_sm = {n for n in NAMES if n.startswith("tc_") and "repack" not in n}
+    path = str(tmp_path / "timeout.jsonl")
+    mm.mm_shutdown()  # fresh peaks: the next options take effect
+    try:
+        # peaks so high that no candidate lands inside the time limit: the
+        # round is not cut short before the 1-SM candidates are measured
+        mm.check(mm.mm_set_option("peak_tflops", "1e9"))
+        mm.check(mm.mm_set_option("peak_gbs", "1e9"))
+        mm.check(mm.mm_set_option("decisions", path))
+        mm.check(mm.mm_set_option("wait_limit_us", "1000"))
+        mm.check(mm.mm_set_option("wait_stall", "1"))
+        c = Case(256, 256, 512, dist="int4", seed=12).device()
+        mm.check(execute(c))
+        c.check(exact=True)
+        rec = _last_decision(path)
+        states = {x["name"]: x["state"] for x in rec["candidates"]}
+        measured = {n for n in one_sm if states.get(n) not in (None, "skipped", "unsupported")}
+        assert measured and all(states[n] == "timeout" for n in measured), states
+        assert rec["fastest"] not in one_sm, rec["fastest"]
+        s = Case(128, 128, 4096, dt=(BF16, BF16, F32), dist="int4", seed=13).device()
+        st = mm.mm_splitk_gemm_noalloc(s.pA, s.pB, s.pC, 128, 128, 4096, s.A.ld, s.B.ld, s.C.ld,
+                                       s.dt, "NN")
+        assert st == mm.MM_OK, mm.mm_last_error()
+        assert mm.mm_splitk_gemm_noalloc_status() == mm.MM_ERR_TIMEOUT
+        assert "gave up" in mm.mm_last_error()
+        mm.check(mm.mm_set_option("wait_stall", "0"))
+        mm.check(mm.mm_set_option("wait_limit_us", "2000000"))
+        for _ in range(2):
+            s.device()
+            mm.check(mm.mm_splitk_gemm_noalloc(s.pA, s.pB, s.pC, 128, 128, 4096, s.A.ld, s.B.ld,
+                                               s.C.ld, s.dt, "NN"))
+            assert mm.mm_splitk_gemm_noalloc_status() == mm.MM_OK
+            s.check(exact=True)
+        i = NAMES.index("tc_128x128_s6")
+        c.device()
+        mm.check(mm.mm_execute_candidate(i, *c.args()))
+        c.check(exact=True)
+    finally:
+        for k in ("peak_tflops", "peak_gbs"):
+            mm.mm_set_option(k, "0")
+        mm.mm_set_option("wait_stall", "0")
+        mm.mm_set_option("wait_limit_us", "2000000")
+        mm.mm_shutdown()  # drop the inflated peaks
