@@ -174,7 +174,8 @@ mm_status mm_cache_save(const char *path);
  *   batch,stride_a,stride_b,stride_c
  * mm_tune_file tunes every recorded problem not yet in the current device's
  * table, on library-allocated synthetic operands of the recorded shape and
- * strides (freed before it returns), and sets *tuned to the number tuned;
+ * strides (pseudo-random values in [-1, 1); freed before it returns), and
+ * sets *tuned to the number tuned;
  * the results can then be written with mm_cache_save.  Runs whether or not
  * the "tuning" option is on.  Errors: MM_ERR_IO if the file cannot be read,
  * MM_ERR_INVALID_ARG for a malformed record, MM_ERR_CUDA, or the tuner's own
@@ -225,6 +226,21 @@ int32_t mm_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64
                 int32_t *group_prio, int32_t *prio);
 /* Name of a group id reported by mm_plan ("gemv", "tensor", "naive"). */
 const char *mm_group_name(int32_t group);
+
+/*
+ * mm_default_candidate -- the candidate a miss that is not tuned runs on the
+ * current device (tuning off, or a pending key whose tuner did not finish in
+ * time; the TunableOp guide's Default, made a heuristic): a shape-class
+ * preference drawn from the GB300 tuning results (M = 1: the streaming
+ * GEMVs; M <= 16: the swapped tensor-core split-K; few tiles and deep K:
+ * split-K; f32: the 1-SM tile; small outputs: the 128 x 64 tile; otherwise
+ * the 2-SM 256 x 256 tile, or the copying form when A's rows are not 16-byte
+ * aligned), then the plan's order, first that supports the problem.  Test and
+ * report hook; the data pointers are taken as 256-byte aligned.  Returns the
+ * candidate index, or -1 for invalid arguments.
+ */
+int32_t mm_default_candidate(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
+                             int64_t ldc, mm_dtypes dt, mm_layout layout, const mm_batch *batch);
 
 /*
  * mm_roofline_limit_ns -- the tuning time limit of the autotune page,

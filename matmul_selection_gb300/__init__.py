@@ -89,6 +89,8 @@ _sig = {
     "mm_plan": (_i32, [_i64, _i64, _i64, _i64, _i64, _i64, mm_dtypes, ctypes.c_int,
                        ctypes.POINTER(mm_batch), _i32, _P32, _P32, _P32, _P32, _P32, _P32]),
     "mm_group_name": (_cp, [_i32]),
+    "mm_default_candidate": (_i32, [_i64, _i64, _i64, _i64, _i64, _i64, mm_dtypes, ctypes.c_int,
+                                    ctypes.POINTER(mm_batch)]),
     "mm_roofline_limit_ns": (ctypes.c_double, [ctypes.c_double] * 6),
     "mm_set_option": (_i32, [_cp, _cp]),
     "mm_get_option": (_i32, [_cp, ctypes.c_char_p, ctypes.c_size_t]),
@@ -254,6 +256,11 @@ def mm_plan(M, N, K, lda, ldb, ldc, dtypes, layout, batch=None, cap=256):
         raise MMError(MM_ERR_INVALID_ARG, mm_last_error())
     keys = ("cand", "group", "tier", "supported", "group_prio", "prio")
     return [{k: arrs[j][i] for j, k in enumerate(keys)} for i in range(n)]
+
+
+def mm_default_candidate(M, N, K, lda, ldb, ldc, dtypes, layout, batch=None):
+    return _lib.mm_default_candidate(M, N, K, lda, ldb, ldc, _dt(dtypes), _layout(layout),
+                                     _batch(batch))
 
 
 def mm_group_name(g):

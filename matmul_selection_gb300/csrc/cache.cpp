@@ -258,8 +258,7 @@ mm_status tune_file(DeviceState &ds, const std::string &path, int *tuned) {
       std::shared_lock<std::shared_mutex> lk(ds.table_mu);
       if (ds.table.count(key)) continue;  // already tuned
     }
-    // synthetic operands of the recorded shape (values do not change the
-    // choice: every candidate computes the same product)
+    // synthetic operands of the recorded shape
     DevBuf a, bb, c;
     struct Release {
       DevBuf &x, &y, &z;
@@ -275,8 +274,11 @@ mm_status tune_file(DeviceState &ds, const std::string &path, int *tuned) {
     mm_status st;
     if ((st = a.ensure(na)) != MM_OK || (st = bb.ensure(nb)) != MM_OK || (st = c.ensure(nc)) != MM_OK)
       return st;
-    MM_CUDA_TRY(cudaMemsetAsync(a.ptr, 0x3c, na, ds.tune_stream));
-    MM_CUDA_TRY(cudaMemsetAsync(bb.ptr, 0x3c, nb, ds.tune_stream));
+    // pseudo-random operands: every candidate computes the same product, but
+    // constant data would let compute-bound candidates run at a lower power
+    if ((st = launch_fill(a.ptr, na / dtype_bytes(p.ta), p.ta, 1u, ds.tune_stream)) != MM_OK ||
+        (st = launch_fill(bb.ptr, nb / dtype_bytes(p.tb), p.tb, 2u, ds.tune_stream)) != MM_OK)
+      return st;
     p.A = a.ptr;
     p.B = bb.ptr;
     p.C = c.ptr;

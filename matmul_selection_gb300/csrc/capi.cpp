@@ -226,6 +226,17 @@ int32_t mm_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64
 
 const char *mm_group_name(int32_t g) { return group_name(g); }
 
+int32_t mm_default_candidate(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
+                             int64_t ldc, mm_dtypes dt, mm_layout layout, const mm_batch *batch) {
+  Problem p;
+  static char dummy[256] __attribute__((aligned(256)));
+  if (make_problem(&p, dummy, dummy, dummy, M, N, K, lda, ldb, ldc, dt, layout, batch) != MM_OK)
+    return -1;
+  DeviceState *ds = nullptr;
+  if (current_device(&ds) != MM_OK) return -1;
+  return default_candidate(make_key(p, get_options().level), p, ds->info);
+}
+
 mm_status mm_set_option(const char *name, const char *value) {
   if (!name || !value) return set_error(MM_ERR_INVALID_ARG, "null option name/value");
   return set_option(name, value);

@@ -283,6 +283,11 @@ struct PlanItem {
   int cand, group, tier, supported, group_prio, prio;
 };
 std::vector<PlanItem> make_plan(const KeyPod &k, const Problem &p, const DeviceInfo &d);
+// The default for a key that is not tuned: the candidates in the order they
+// are tried (a shape-class preference, then the plan), and the first of them
+// that supports the problem.
+std::vector<int> default_order(const KeyPod &k, const Problem &p, const DeviceInfo &d);
+int default_candidate(const KeyPod &k, const Problem &p, const DeviceInfo &d);
 
 // Launch one candidate with fault injection and counting applied.
 mm_status launch_candidate(int index, const Problem &p, LaunchCtx &ctx);
@@ -290,6 +295,8 @@ mm_status launch_candidate(int index, const Problem &p, LaunchCtx &ctx);
 // ---------------------------------------------------------------- kernels
 mm_status launch_naive(const Problem &p, cudaStream_t s);
 mm_status launch_l2_flush(void *buf, size_t bytes, cudaStream_t s);
+// Pseudo-random values in [-1, 1) of type dtype (offline tuning's operands).
+mm_status launch_fill(void *buf, size_t elems, int dtype, unsigned seed, cudaStream_t s);
 mm_status launch_empty(cudaStream_t s);
 mm_status launch_delay(unsigned long long ns, cudaStream_t s);
 mm_status launch_copy_probe(const void *src, void *dst, size_t bytes, cudaStream_t s);

@@ -67,6 +67,7 @@ struct RepackCfg {
 };
 const RepackCfg kRepackCfgs[] = {
     {"tc2_repack_256x256", "tc2_256x256_s7", false},
+    {"tc2_repack_256x224", "tc2_256x224_s7", false},
     {"tc_repack_128x128", "tc_128x128_s6", false},
     {"tc_repack_128x64", "tc_128x64_s8", false},
     {"tc_repack_splitk_128x128", "tc_splitk_128x128_s7", false},

@@ -929,13 +929,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     const __grid_constant__ CUtensorMap tmBh, const TcParams p) {
   pdl_launch_dependents();
   constexpr int BNH = BN / 2;                 // B columns held by each CTA
+  // B's smem slot: a whole number of 64-column boxes (BN = 224: two boxes,
+  // the last 16 columns of the second unused by the MMA)
+  constexpr int BNH_SLOT = (BNH + 63) / 64 * 64;
   constexpr uint32_t A_BYTES = BM * 128;
-  constexpr uint32_t B_BYTES = BNH * 128;
+  constexpr uint32_t B_BYTES = BNH_SLOT * 128;
   constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
   constexpr int BK = 128 / ES;
   constexpr int UMMA_K = 32 / ES;
   constexpr int KSTEPS = BK / UMMA_K;
-  constexpr uint32_t TMEM_COLS = 2 * BN;
+  // two accumulators of BN columns, allocated as a power of two
+  constexpr uint32_t TMEM_COLS = 2 * BN <= 256 ? 256 : 512;
   constexpr int ATOM = 128 / ES;
   constexpr int PAIR_M = 2 * BM;
 
@@ -993,7 +997,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (!p.b_mn) tma_prefetch_3d(&tmB, kb * BK, n0, b);  // box of BN/2 columns: covers this share
         else if (p.b_4d && nh == BNH) tma_prefetch_4d(&tmB, 0, kb * BK, n0 / ATOM, b);
         else
-          for (int j = 0; j < nh / ATOM; ++j)
+          for (int j = 0; j < (nh + ATOM - 1) / ATOM; ++j)
             tma_prefetch_3d(p.b_4d ? &tmBh : &tmB, n0 + j * ATOM, kb * BK, b);
       }
     }
@@ -1027,7 +1031,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int nh = w / 2;    // B columns this CTA loads for the unit
         const int m0 = tm * PAIR_M + (int)pos * BM;
         const int n0 = t0 + (int)pos * nh;
-        const uint32_t tx = 2 * (A_BYTES + (uint32_t)nh * 128);
+        // bytes both CTAs' copies bring (an MN-major B comes in whole boxes)
+        const uint32_t nh_bytes = (uint32_t)(p.b_mn ? (nh + ATOM - 1) / ATOM * ATOM : nh) * 128;
+        const uint32_t tx = 2 * (A_BYTES + nh_bytes);
         for (int kb = 0; kb < p.num_kb; ++kb) {
           if (!warp_wait(empty0 + 8 * stage, phase ^ 1, abort_flag, p.err, kErrProducer,
                          p.timeout_ns)) {
@@ -1052,7 +1058,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           } else if (p.b_4d && nh == BNH) {
             tma_load_4d_pair(sb, &tmB, lfb, 0, kb * BK, n0 / ATOM, b);
           } else {  // with a 4-D map in tmB, tmBh holds the per-box 3-D map
-            for (int j = 0; j < nh / ATOM; ++j)
+            for (int j = 0; j < (nh + ATOM - 1) / ATOM; ++j)
               tma_load_3d_pair(sb + j * p.b_box_stride, p.b_4d ? &tmBh : &tmB, lfb, n0 + j * ATOM,
                                kb * BK, b);
           }
@@ -1283,6 +1289,9 @@ struct TcCfg {
 // fastest on large problems come first.
 const TcCfg kCfgs[] = {
     {"tc2_256x256_s7", 256, 7, false, true},
+    // 224 columns: 19 column tiles for N = 4096, so four row tiles of 256
+    // make one full wave of 76 pairs (the 1000-row products)
+    {"tc2_256x224_s7", 224, 7, false, true},
     {"tc2_256x128_s8", 128, 8, false, true},
     {"tc_128x256_s4", 256, 4, false, false},
     {"tc_128x128_s6", 128, 6, false, false},
@@ -1299,7 +1308,7 @@ size_t smem_bytes(int bn, int stages, bool sk) {
 
 size_t smem_bytes_cfg(const TcCfg &c) {
   if (!c.pair) return smem_bytes(c.bn, c.stages, c.splitk);
-  return (size_t)c.stages * (BM * 128 + (c.bn / 2) * 128) + kPairSlack + 1024 + 256;
+  return (size_t)c.stages * (BM * 128 + ((c.bn / 2 + 63) / 64 * 64) * 128) + kPairSlack + 1024 + 256;
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -1441,6 +1450,7 @@ struct PairKernel {
 template <int ES>
 mm_status pair_capacity(int cfg, int *max_clusters) {
   if (kCfgs[cfg].bn == 256) return PairKernel<256, 7, ES>::capacity(max_clusters);
+  if (kCfgs[cfg].bn == 224) return PairKernel<224, 7, ES>::capacity(max_clusters);
   return PairKernel<128, 8, ES>::capacity(max_clusters);
 }
 
@@ -1449,6 +1459,7 @@ mm_status dispatch_pair(int cfg, const CUtensorMap &ma, const CUtensorMap &mb,
                         const CUtensorMap &mbh, const TcParams &tp, int clusters,
                         cudaStream_t s) {
   if (kCfgs[cfg].bn == 256) return PairKernel<256, 7, ES>::launch(ma, mb, mbh, tp, clusters, s);
+  if (kCfgs[cfg].bn == 224) return PairKernel<224, 7, ES>::launch(ma, mb, mbh, tp, clusters, s);
   return PairKernel<128, 8, ES>::launch(ma, mb, mbh, tp, clusters, s);
 }
 
@@ -1818,7 +1829,7 @@ mm_status launch_tc_impl(const Problem &p, LaunchCtx &ctx, int cfg, bool c_trans
   tp.a_kstep = tp.a_mn ? (uint32_t)(umma_k * 128) >> 4 : 32u >> 4;
   tp.b_kstep = tp.b_mn ? (uint32_t)(umma_k * 128) >> 4 : 32u >> 4;
   tp.a_boxes = tp.a_mn ? BM / atom : 1;
-  tp.b_boxes = tp.b_mn ? bn_cta / atom : 1;
+  tp.b_boxes = tp.b_mn ? (bn_cta + atom - 1) / atom : 1;
   tp.a_box_stride = mn_atom_bytes;
   tp.b_box_stride = mn_atom_bytes;
   if (c.pair) {

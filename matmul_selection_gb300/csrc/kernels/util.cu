@@ -37,6 +37,32 @@ __global__ void copy_kernel(const uint4 *__restrict__ src, uint4 *__restrict__ d
   for (; i < n16; i += stride) dst[i] = src[i];
 }
 
+// Fills n elements of type t with values in [-1, 1): element i gets the top
+// bits of a 32-bit integer hash of (seed, i) (the lowbias32 mixer), so that
+// offline tuning times its candidates on data that toggles like real operands
+// (constant data lets the tensor cores run cooler and faster).
+__global__ void fill_kernel(void *buf, size_t n, int t, unsigned seed) {
+  pdl_launch_dependents();
+  pdl_wait();
+  size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const size_t stride = (size_t)gridDim.x * blockDim.x;
+  for (; i < n; i += stride) {
+    uint32_t h = (uint32_t)i * 0x9E3779B9u ^ seed ^ (uint32_t)(i >> 32);
+    h ^= h >> 16;
+    h *= 0x7feb352du;
+    h ^= h >> 15;
+    h *= 0x846ca68bu;
+    h ^= h >> 16;
+    const float v = (float)(h >> 8) * (1.0f / 8388608.0f) - 1.0f;
+    if (t == MM_F32)
+      static_cast<float *>(buf)[i] = v;
+    else if (t == MM_BF16)
+      static_cast<__nv_bfloat16 *>(buf)[i] = __float2bfloat16_rn(v);
+    else
+      static_cast<__half *>(buf)[i] = __float2half_rn(v);
+  }
+}
+
 // Occupies the stream for about `ns` nanoseconds (one thread, bounded by
 // %globaltimer), so that work enqueued behind it meanwhile runs back to back.
 __global__ void delay_kernel(unsigned long long ns) {
@@ -84,6 +110,12 @@ mm_status launch_delay(unsigned long long ns, cudaStream_t s) {
   if (ns > 10000000ull) ns = 10000000ull;  // never more than 10 ms
   cudaError_t e = launch_pdl(delay_kernel, dim3(1), dim3(1), 0, s, dim3(1), ns);
   return e == cudaSuccess ? MM_OK : cuda_error(e, "delay_kernel launch");
+}
+
+mm_status launch_fill(void *buf, size_t elems, int dtype, unsigned seed, cudaStream_t s) {
+  if (!elems) return MM_OK;
+  cudaError_t e = launch_pdl(fill_kernel, dim3(2048), dim3(256), 0, s, dim3(1), buf, elems, dtype, seed);
+  return e == cudaSuccess ? MM_OK : cuda_error(e, "fill_kernel launch");
 }
 
 mm_status launch_l2_flush(void *buf, size_t bytes, cudaStream_t s) {

@@ -177,6 +177,54 @@ std::vector<PlanItem> make_plan(const KeyPod &k, const Problem &p, const DeviceI
   return plan;
 }
 
+// The default for a key that is not tuned (tuning off, or a pending key whose
+// tuner did not finish in time): a preference list by shape class, each entry
+// the candidate that won that class on a GB300 (the committed tuning table),
+// then the plan's order; the first that supports the problem is taken.
+//   m = 1                  : gemv_n_stream / gemv_t_stream (B row-major / transposed)
+//   m <= 16                : the swapped tensor-core split-K (on a copy of A if
+//                            A's rows are not 16-byte aligned)
+//   few tiles, deep k      : split-K (the split-K group rule)
+//   f32 inputs             : tc_128x256_s4, tc_128x128_s6
+//   small outputs          : tc_128x64_s8 (m*n <= 512 x 512: latency)
+//   otherwise              : tc2_256x256_s7, or its copying form
+std::vector<int> default_order(const KeyPod &k, const Problem &p, const DeviceInfo &d) {
+  std::vector<const char *> pref;
+  const bool aligned_a = k.lhs_stride >= 4;
+  if (k.m <= 1) {
+    pref = {p.bt ? "gemv_t_stream" : "gemv_n_stream"};
+  } else if (k.m <= 16) {
+    pref = {aligned_a ? "gemv_swap_tc_splitk_128x64_s8" : "gemv_swap_tc_repack_splitk_128x64"};
+  } else if (prio_splitk(k, d) == PRIORITY_HIGH) {
+    pref = {aligned_a ? "tc_splitk_128x128_s7" : "tc_repack_splitk_128x128"};
+  } else if (p.ta == MM_F32) {
+    pref = {"tc_128x256_s4", "tc_128x128_s6"};
+  } else if (k.m * k.n <= 512 * 512 && k.batch <= 1) {
+    pref = {"tc_128x64_s8"};
+  } else if (k.batch > 1) {
+    pref = {"tc_128x256_s4"};
+  } else {
+    pref = {aligned_a ? "tc2_256x256_s7" : "tc2_repack_256x256"};
+  }
+  std::vector<int> order;
+  const auto &reg = registry();
+  for (const char *name : pref)
+    for (int i = 0; i < (int)reg.size(); ++i)
+      if (reg[i].name == name) order.push_back(i);
+  for (const PlanItem &it : make_plan(k, p, d))
+    if (std::find(order.begin(), order.end(), it.cand) == order.end()) order.push_back(it.cand);
+  return order;
+}
+
+int default_candidate(const KeyPod &k, const Problem &p, const DeviceInfo &d) {
+  const auto &reg = registry();
+  for (int c : default_order(k, p, d)) {
+    std::string why;
+    if (reg[c].supports(p, d, reg[c].cfg, &why)) return c;
+  }
+  return 0;
+}
+
 // Host-side fault injection: "<candidate name>:error" makes that candidate's
 // launch fail without launching anything.
 static bool fault_error(const std::string &spec, const std::string &name) {

@@ -598,15 +598,16 @@ mm_status run_entry(DeviceState &ds, const TableEntry &e, const Problem &p, cuda
 }
 
 // The default for a miss that is not tuned (tuning off, a pending key whose
-// tuner did not finish in time): the first candidate of the key's plan that
-// supports the problem, i.e. the one the tuner would measure first, instead
-// of the naive kernel; the next one if its launch fails.
+// tuner did not finish in time): the shape-class heuristic's choice, then the
+// key's plan, first that supports the problem; the next one if a launch fails.
 mm_status launch_default(DeviceState &ds, const KeyPod &key, const Problem &p, LaunchCtx &ctx,
                          ExecResult *res) {
-  for (const PlanItem &it : make_plan(key, p, ds.info)) {
-    if (!it.supported) continue;
-    if (launch_candidate(it.cand, p, ctx) == MM_OK) {
-      if (res) res->candidate = it.cand;
+  const auto &reg = registry();
+  for (int c : default_order(key, p, ds.info)) {
+    std::string why;
+    if (!reg[c].supports(p, ds.info, reg[c].cfg, &why)) continue;
+    if (launch_candidate(c, p, ctx) == MM_OK) {
+      if (res) res->candidate = c;
       return MM_OK;
     }
   }

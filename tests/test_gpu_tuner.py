@@ -164,18 +164,41 @@ def test_hand_edits_default_and_unknown_name(tmp_path):
 
 
 def test_tuning_disabled_runs_default():
-    """With tuning off a miss runs the plan's first supported candidate (the
-    one the tuner would measure first), records nothing and measures nothing."""
+    """With tuning off a miss runs the default candidate (the shape-class
+    heuristic's choice), records nothing and measures nothing."""
     mm.check(mm.mm_set_option("tuning", "0"))
-    for shape in [(96, 80, 200), (1, 512, 512), (4096, 256, 64)]:
+    for shape in [(96, 80, 200), (1, 512, 512), (4096, 256, 64), (8, 1024, 1024)]:
         c = Case(*shape, dist="int4").device()
-        items = mm.mm_plan(*shape, shape[2], shape[1], shape[1], c.dt, "NN")
-        first = next(it["cand"] for it in items if it["supported"])
+        first = mm.mm_default_candidate(*shape, shape[2], shape[1], shape[1], c.dt, "NN")
+        assert first >= 0
         n0 = mm.mm_candidate_launches(first)
         mm.check(execute(c))
         c.check(exact=True)
         assert mm.mm_candidate_launches(first) == n0 + 1, NAMES[first]
     assert mm.mm_cache_size() == 0 and mm.mm_get_stats()["tunes"] == 0
+
+
+@pytest.mark.parametrize("shape,layout,pad,dt,batch,want", [
+    ((1, 4096, 4096), "NN", 0, (BF16, BF16, BF16), None, "gemv_n_stream"),
+    ((1, 4096, 4096), "NT", 0, (BF16, BF16, BF16), None, "gemv_t_stream"),
+    ((16, 4096, 4096), "NN", 0, (BF16, BF16, BF16), None, "gemv_swap_tc_splitk_128x64_s8"),
+    ((16, 4096, 4096), "NN", 4, (BF16, BF16, BF16), None, "gemv_swap_tc_repack_splitk_128x64"),
+    ((128, 128, 65536), "NN", 0, (BF16, BF16, BF16), None, "tc_splitk_128x128_s7"),
+    ((4096, 4096, 4096), "NN", 0, (BF16, BF16, BF16), None, "tc2_256x256_s7"),
+    ((8192, 4096, 4096), "NN", 4, (BF16, BF16, BF16), None, "tc2_repack_256x256"),
+    ((25088, 4096, 64), "NT", 0, (F32, F32, F32), None, "tc_128x256_s4"),
+    ((256, 256, 256), "NN", 0, (BF16, BF16, F32), None, "tc_128x64_s8"),
+    ((512, 512, 512), "NN", 0, (BF16, BF16, F32), (32, 512 * 512, 512 * 512, 512 * 512),
+     "tc_128x256_s4"),
+])
+def test_default_heuristic_matches_tuned_winners(shape, layout, pad, dt, batch, want):
+    """The default for an untuned key is the candidate that won that shape
+    class in the committed GB300 table."""
+    M, N, K = shape
+    lda = (M if layout[0] == "T" else K) + pad
+    ldb = K if layout[1] == "T" else N
+    got = mm.mm_default_candidate(M, N, K, lda, ldb, N, dt, layout, batch)
+    assert NAMES[got] == want
 
 
 @pytest.mark.parametrize("mode", ["error", "nan"])
