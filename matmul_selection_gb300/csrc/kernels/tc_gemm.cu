@@ -45,6 +45,9 @@ namespace {
 constexpr int BM = 128;
 // 7 warps: A copies, MMA, 4 epilogue warps, B copies
 constexpr int kTcThreads = 224;
+// 2-SM kernel with A copied by cp.async (rows TMA cannot address): 4 more
+// warps (7..10) copy A, warp 0 relays the copies' completion
+constexpr int kTcThreadsAsyncA = 352;
 // 1-SM kernel shared memory after the ring: two 4 KB output staging boxes for
 // each epilogue warp (32 rows x 128 bytes, 128-byte swizzle; also the fallback
 // store path's [32][33] transpose scratch), then the barriers
@@ -80,6 +83,12 @@ struct TcParams {
   // test hook: the MMA warp first waits on a barrier nothing arrives on, so
   // that the wait limit runs out and the kernel's abort path runs
   int stall_wait;
+  // 2-SM kernel, A copied by cp.async: A itself (K-major), its row and batch
+  // strides in bytes, and the piece size (8 or 4 bytes: the largest that
+  // divides the base address and both strides)
+  const char *a_ptr;
+  int64_t a_row_bytes, a_batch_bytes;
+  int a_piece;
   // 1-SM kernel: C written by TMA bulk-tensor stores (tmC valid); with
   // splits > 1, tmC maps the fp32 workspace as [splits * batch][M][N]
   int c_tma;
@@ -127,6 +136,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// mbarrier wait with acquire semantics at cluster scope (the arrival may be a
+// release by the other CTA of the pair).
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 __device__ __forceinline__ uint64_t global_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -137,13 +160,20 @@ __device__ __forceinline__ uint64_t global_ns() {
 // lane polls; the result is warp-uniform).  Gives up (false) when the shared
 // abort flag is raised or after timeout_ns, raising the flag and recording
 // `code` in the error word.
+template <bool CLUSTER = false>
+__device__ __forceinline__ bool mbar_try_wait_scoped(uint32_t bar, uint32_t parity) {
+  return CLUSTER ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity);
+}
+// CLUSTER: acquire at cluster scope (for arrivals the other CTA of a pair
+// releases).
+template <bool CLUSTER = false>
 __device__ __noinline__ bool warp_wait_slow(uint32_t bar, uint32_t parity, volatile int *abort_flag,
                                             int *err, int code, uint64_t timeout_ns) {
   const uint64_t t0 = global_ns();
   while (true) {
 #pragma unroll 1
     for (int i = 0; i < 32; ++i)
-      if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
+      if (__all_sync(0xffffffffu, mbar_try_wait_scoped<CLUSTER>(bar, parity))) return true;
     int stop = 0;
     if ((threadIdx.x & 31) == 0) {
       if (*abort_flag) {
@@ -157,10 +187,11 @@ __device__ __noinline__ bool warp_wait_slow(uint32_t bar, uint32_t parity, volat
     if (__shfl_sync(0xffffffffu, stop, 0)) return false;
   }
 }
+template <bool CLUSTER = false>
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag,
                                           int *err, int code, uint64_t timeout_ns) {
-  if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
-  return warp_wait_slow(bar, parity, abort_flag, err, code, timeout_ns);
+  if (__all_sync(0xffffffffu, mbar_try_wait_scoped<CLUSTER>(bar, parity))) return true;
+  return warp_wait_slow<CLUSTER>(bar, parity, abort_flag, err, code, timeout_ns);
 }
 
 // Bounded wait that ignores the abort flag: used at the end to let copies and
@@ -250,6 +281,11 @@ __device__ __forceinline__ void tma_store_wait_all() {
 // Generic-proxy writes to shared memory visible to the async proxy (TMA).
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// L2 prefetch of `bytes` (a multiple of 16) at a 16-byte aligned address.
+__device__ __forceinline__ void prefetch_l2_bulk(const void *p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
 
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap *map) {
@@ -786,6 +822,57 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (warp == 1) tmem_dealloc(tmem_base, TMEM_COLS);
 }
 
+// ---------------------------------------------------------------- cp.async copies of A
+// One piece of `BYTES` (8 or 4) bytes from global to shared memory; the bytes
+// past `valid` (0..BYTES) are zero-filled and not read.
+template <int BYTES>
+__device__ __forceinline__ void cp_async_piece(uint32_t dst, const void *src, uint32_t valid) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], %2, %3;" ::"r"(dst), "l"(src), "n"(BYTES),
+               "r"(valid)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+// This thread's cp.async groups, all but the newest N, have landed.
+template <int N>
+__device__ __forceinline__ void cp_async_wait_group() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+// This thread's generic-proxy writes to shared memory (its landed cp.async
+// copies) ordered before later async-proxy reads (the tensor cores of either
+// CTA of the pair).
+__device__ __forceinline__ void fence_proxy_async_all() {
+  asm volatile("fence.proxy.async;" ::: "memory");
+}
+
+// 128 rows x 128 bytes of A (K block kb of rows m0..m0+127, K-major) into a
+// stage laid out as the 128-byte-swizzled K-major tile the MMA reads (16-byte
+// chunk j of row r at r * 128 + ((j ^ (r % 8)) << 4)).  Thread t of the 128
+// copies piece t % P of rows t / P, t / P + 128 / P, ... (P pieces a row), so
+// a warp reads whole 128-byte row segments.  Rows past M and bytes past K are
+// zero-filled.
+template <int BYTES, int ES>
+__device__ __forceinline__ void copy_a_stage(const TcParams &p, uint32_t sa, int m0, int b, int kb,
+                                             int t) {
+  constexpr int P = 128 / BYTES;  // pieces a row
+  const int pi = t % P;
+  const int boff = pi * BYTES;     // byte of the piece in the row's 128
+  const int64_t kbyte = (int64_t)kb * 128 + boff;
+  const int64_t krow = (int64_t)p.K * ES;
+  const uint32_t kvalid = kbyte >= krow ? 0u : (uint32_t)(krow - kbyte < BYTES ? krow - kbyte : BYTES);
+  const char *base = p.a_ptr + (int64_t)b * p.a_batch_bytes + kbyte;
+  const uint32_t chunk = (uint32_t)(boff >> 4), half = (uint32_t)(boff & 15);
+#pragma unroll 4
+  for (int r = t / P; r < BM; r += 128 / P) {
+    const int m = m0 + r;
+    const uint32_t valid = m < p.M ? kvalid : 0u;
+    const void *src = valid ? base + (int64_t)m * p.a_row_bytes : p.a_ptr;
+    const uint32_t dst = sa + (uint32_t)r * 128u + (((chunk ^ (uint32_t)(r & 7)) << 4) | half);
+    cp_async_piece<BYTES>(dst, src, valid);
+  }
+}
+
 // ---------------------------------------------------------------- 2-SM kernel
 // The same pipeline on a CTA pair (cluster of 2) with tcgen05.mma.cta_group::2:
 // one MMA instruction computes a 256 x BN tile; each CTA holds 128 rows of A
@@ -922,8 +1009,14 @@ __device__ __forceinline__ void pair_unit(const TcParams &p, int u, int bn, int 
   nw = half < 0 ? bn : bn / 2;
 }
 
-template <int BN, int STAGES, int ES>
-__global__ void __launch_bounds__(kTcThreads, 1)
+// AL: A is copied by cp.async (warps 7..10, 128-byte-swizzled as TMA would
+// have laid it out) instead of TMA, for rows that TMA cannot address (a
+// leading dimension or base that is not a multiple of 16 bytes).  Each CTA's
+// copies complete on a local barrier; warp 0 waits for it, fences the writes
+// to the async proxy and arrives on the leader's full barrier (which then
+// expects the arming, both CTAs' A arrivals and both CTAs' B bytes).
+template <int BN, int STAGES, int ES, bool AL>
+__global__ void __launch_bounds__(AL ? kTcThreadsAsyncA : kTcThreads, 1)
     tc2_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                     const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmBh, const TcParams p) {
@@ -952,7 +1045,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const uint32_t tfull0 = empty0 + 8 * STAGES;
   const uint32_t tempty0 = tfull0 + 16;
   const uint32_t drain = tempty0 + 16;
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * STAGES + 5);
+  const uint32_t afull0 = drain + 8;  // AL: this CTA's A copies of a stage landed
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * STAGES + 5 + (AL ? STAGES : 0));
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -963,8 +1057,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(full0 + 8 * s, 1);
+      mbar_init(full0 + 8 * s, AL ? 3 : 1);  // (AL: the arming and both CTAs' A relays)
       mbar_init(empty0 + 8 * s, 1);  // one commit from the leader
+      if (AL) mbar_init(afull0 + 8 * s, 128);  // each copying thread's cp.async arrival
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull0 + 8 * a, 1);
@@ -989,6 +1084,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int kb1 = min(p.num_kb, (int)(kPrefetchBytes / STAGE_BYTES));
     for (int kb = 0; kb < kb1; ++kb) {
       if (warp == 0) {
+        if (AL) break;  // (the copying warps prefetch A)
         if (!p.a_mn) tma_prefetch_3d(&tmA, kb * BK, m0, b);
         else if (p.a_4d) tma_prefetch_4d(&tmA, 0, kb * BK, m0 / ATOM, b);
         else
@@ -1000,6 +1096,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           for (int j = 0; j < (nh + ATOM - 1) / ATOM; ++j)
             tma_prefetch_3d(p.b_4d ? &tmBh : &tmB, n0 + j * ATOM, kb * BK, b);
       }
+    }
+  }
+  if (AL && warp >= 7 && cid < p.total_units) {
+    // the copying threads prefetch the first K blocks of their rows of the
+    // first unit into L2 (whole 16-byte granules inside each row)
+    int tm, t0, b, w;
+    pair_unit(p, cid, BN, tm, t0, b, w);
+    const int m = tm * PAIR_M + (int)pos * BM + (int)threadIdx.x - 32 * 7;
+    if (m < p.M) {
+      const uintptr_t row = reinterpret_cast<uintptr_t>(p.a_ptr + (int64_t)b * p.a_batch_bytes +
+                                                        (int64_t)m * p.a_row_bytes);
+      const int64_t pf = (int64_t)(kPrefetchBytes / STAGE_BYTES) * 128, krow = (int64_t)p.K * ES;
+      const int64_t len = krow < pf ? krow : pf;
+      const uintptr_t lo = (row + 15) & ~(uintptr_t)15, hi = (row + (uintptr_t)len) & ~(uintptr_t)15;
+      if (hi > lo) prefetch_l2_bulk(reinterpret_cast<const void *>(lo), (uint32_t)(hi - lo));
     }
   }
   if (warp == 1) {
@@ -1033,7 +1144,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int n0 = t0 + (int)pos * nh;
         // bytes both CTAs' copies bring (an MN-major B comes in whole boxes)
         const uint32_t nh_bytes = (uint32_t)(p.b_mn ? (nh + ATOM - 1) / ATOM * ATOM : nh) * 128;
-        const uint32_t tx = 2 * (A_BYTES + nh_bytes);
+        const uint32_t tx = 2 * ((AL ? 0u : A_BYTES) + nh_bytes);
         for (int kb = 0; kb < p.num_kb; ++kb) {
           if (!warp_wait(empty0 + 8 * stage, phase ^ 1, abort_flag, p.err, kErrProducer,
                          p.timeout_ns)) {
@@ -1045,7 +1156,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           const uint32_t sb = sa + A_BYTES;
           if (copy_a) {
             if (leader) mbar_expect_tx(full0 + 8 * stage, tx);
-            if (!p.a_mn) {
+            if (AL) {
+              // relay: this CTA's A copies of the stage have landed
+              if (!warp_wait(afull0 + 8 * stage, phase, abort_flag, p.err, kErrProducer,
+                             p.timeout_ns)) {
+                ok = false;
+                break;
+              }
+              if (lane == 0) {
+                if (leader)
+                  mbar_arrive(full0 + 8 * stage);
+                else
+                  mbar_arrive_cluster(lfb);
+              }
+              __syncwarp();
+            } else if (!p.a_mn) {
               tma_load_3d_pair(sa, &tmA, lfb, kb * BK, m0, b);
             } else if (p.a_4d) {
               tma_load_4d_pair(sa, &tmA, lfb, 0, kb * BK, m0 / ATOM, b);
@@ -1095,7 +1220,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
         for (int kb = 0; kb < p.num_kb; ++kb) {
-          if (!warp_wait(full0 + 8 * stage, phase, abort_flag, p.err, kErrMma, p.timeout_ns)) {
+          // (AL: the other CTA's A relay is a release at cluster scope)
+          if (!warp_wait<AL>(full0 + 8 * stage, phase, abort_flag, p.err, kErrMma, p.timeout_ns)) {
             ok = false;
             break;
           }
@@ -1125,6 +1251,53 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       wait_drain(drain, 0, p.err, kErrDrain, kDrainTimeoutNs);
     }
     __syncwarp();
+  } else if (AL && warp >= 7) {
+    // ------------------------------------------------------------ A copies (both CTAs)
+    // One cp.async group a fill.  Once a fill's group has landed (kLag fills
+    // later, so that about kLag + 1 fills are in flight) the thread fences its
+    // writes to the async proxy and arrives on the stage's afull barrier
+    // (128 arrivals).  kLag < STAGES - 1: issuing fill f + kLag needs only
+    // fill f + kLag - STAGES consumed, which precedes fill f.
+    constexpr int kLag = 3;
+    static_assert(kLag < STAGES - 1, "the copies' lag must stay inside the ring");
+    const int t = (int)threadIdx.x - 32 * 7;
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    int nfill = 0;
+    for (int u = cid; u < p.total_units && ok; u += ncl) {
+      int tm, t0, b, w;
+      pair_unit(p, u, BN, tm, t0, b, w);
+      const int m0 = tm * PAIR_M + (int)pos * BM;
+      for (int kb = 0; kb < p.num_kb; ++kb) {
+        if (!warp_wait(empty0 + 8 * stage, phase ^ 1, abort_flag, p.err, kErrProducer,
+                       p.timeout_ns)) {
+          ok = false;
+          break;
+        }
+        const uint32_t sa = smem_u32(smem + stage * STAGE_BYTES);
+        if (p.a_piece == 8)
+          copy_a_stage<8, ES>(p, sa, m0, b, kb, t);
+        else
+          copy_a_stage<4, ES>(p, sa, m0, b, kb, t);
+        cp_async_commit();
+        if (nfill >= kLag) {
+          cp_async_wait_group<kLag>();
+          fence_proxy_async_all();
+          mbar_arrive(afull0 + 8 * ((nfill - kLag) % STAGES));
+        }
+        ++nfill;
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+    }
+    cp_async_wait_group<0>();  // no copy in flight when shared memory is released
+    if (ok) {
+      fence_proxy_async_all();
+      for (int f = max(0, nfill - kLag); f < nfill; ++f) mbar_arrive(afull0 + 8 * (f % STAGES));
+    }
   } else {
     // ------------------------------------------------------------ epilogue (both CTAs)
     const int q = warp & 3;
@@ -1282,22 +1455,26 @@ struct TcCfg {
   int stages;
   bool splitk;
   bool pair;    // 2-SM (cta_group::2) kernel, tile M = 256
+  bool async_a;  // 2-SM kernel with A copied by cp.async (A rows TMA cannot address)
 };
 
 // In the tuner's priority order: where a round ends early (a candidate within
 // the roofline limit), the earlier entry wins, so the configurations that are
 // fastest on large problems come first.
 const TcCfg kCfgs[] = {
-    {"tc2_256x256_s7", 256, 7, false, true},
+    {"tc2_256x256_s7", 256, 7, false, true, false},
     // 224 columns: 19 column tiles for N = 4096, so four row tiles of 256
     // make one full wave of 76 pairs (the 1000-row products)
-    {"tc2_256x224_s7", 224, 7, false, true},
-    {"tc2_256x128_s8", 128, 8, false, true},
-    {"tc_128x256_s4", 256, 4, false, false},
-    {"tc_128x128_s6", 128, 6, false, false},
-    {"tc_128x64_s8", 64, 8, false, false},
-    {"tc_splitk_128x128_s7", 128, 7, true, false},
-    {"tc_splitk_128x64_s8", 64, 8, true, false},
+    {"tc2_256x224_s7", 224, 7, false, true, false},
+    {"tc2_256x128_s8", 128, 8, false, true, false},
+    // A rows whose leading dimension or base is not a multiple of 16 bytes
+    // (lda = 4100 bf16, say), read in place by cp.async: no copy of A
+    {"tc2_cpasync_256x256_s7", 256, 7, false, true, true},
+    {"tc_128x256_s4", 256, 4, false, false, false},
+    {"tc_128x128_s6", 128, 6, false, false, false},
+    {"tc_128x64_s8", 64, 8, false, false, false},
+    {"tc_splitk_128x128_s7", 128, 7, true, false, false},
+    {"tc_splitk_128x64_s8", 64, 8, true, false, false},
 };
 
 // 1-SM kernel: the ring, the epilogue staging (split-K configurations stage
@@ -1399,15 +1576,16 @@ mm_status launch_kernel(const CUtensorMap &ma, const CUtensorMap &mb, const CUte
   return MM_OK;
 }
 
-template <int BN, int STAGES, int ES>
+template <int BN, int STAGES, int ES, bool AL>
 struct PairKernel {
+  static constexpr int kThreads = AL ? kTcThreadsAsyncA : kTcThreads;
   static cudaLaunchConfig_t config(size_t smem, cudaStream_t s, cudaLaunchAttribute *attr) {
     cudaLaunchConfig_t lc = {};
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
-    lc.blockDim = dim3(kTcThreads);
+    lc.blockDim = dim3(kThreads);
     lc.dynamicSmemBytes = smem;
     lc.stream = s;
     lc.attrs = attr;
@@ -1415,7 +1593,7 @@ struct PairKernel {
     return lc;
   }
   static size_t smem() {
-    const TcCfg shape{"", BN, STAGES, false, true};
+    const TcCfg shape{"", BN, STAGES, false, true, AL};
     return smem_bytes_cfg(shape);
   }
   // Set-up once: shared-memory attribute and how many pairs fit at once.
@@ -1424,7 +1602,7 @@ struct PairKernel {
     static cudaError_t err = cudaSuccess;
     static int clusters = 0;
     std::call_once(once, [] {
-      auto kern = tc2_gemm_kernel<BN, STAGES, ES>;
+      auto kern = tc2_gemm_kernel<BN, STAGES, ES, AL>;
       err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem());
       if (err == cudaSuccess) {
         cudaLaunchAttribute attr[1];
@@ -1440,8 +1618,8 @@ struct PairKernel {
   }
   static mm_status launch(const CUtensorMap &ma, const CUtensorMap &mb, const CUtensorMap &mbh,
                           const TcParams &tp, int clusters, cudaStream_t s) {
-    cudaError_t e = launch_pdl(tc2_gemm_kernel<BN, STAGES, ES>, dim3((unsigned)(2 * clusters)),
-                               dim3(kTcThreads), smem(), s, dim3(2), ma, mb, mbh, tp);
+    cudaError_t e = launch_pdl(tc2_gemm_kernel<BN, STAGES, ES, AL>, dim3((unsigned)(2 * clusters)),
+                               dim3(kThreads), smem(), s, dim3(2), ma, mb, mbh, tp);
     if (e != cudaSuccess) return cuda_error(e, "tc2_gemm_kernel launch");
     return MM_OK;
   }
@@ -1449,18 +1627,21 @@ struct PairKernel {
 
 template <int ES>
 mm_status pair_capacity(int cfg, int *max_clusters) {
-  if (kCfgs[cfg].bn == 256) return PairKernel<256, 7, ES>::capacity(max_clusters);
-  if (kCfgs[cfg].bn == 224) return PairKernel<224, 7, ES>::capacity(max_clusters);
-  return PairKernel<128, 8, ES>::capacity(max_clusters);
+  if (kCfgs[cfg].async_a) return PairKernel<256, 7, ES, true>::capacity(max_clusters);
+  if (kCfgs[cfg].bn == 256) return PairKernel<256, 7, ES, false>::capacity(max_clusters);
+  if (kCfgs[cfg].bn == 224) return PairKernel<224, 7, ES, false>::capacity(max_clusters);
+  return PairKernel<128, 8, ES, false>::capacity(max_clusters);
 }
 
 template <int ES>
 mm_status dispatch_pair(int cfg, const CUtensorMap &ma, const CUtensorMap &mb,
                         const CUtensorMap &mbh, const TcParams &tp, int clusters,
                         cudaStream_t s) {
-  if (kCfgs[cfg].bn == 256) return PairKernel<256, 7, ES>::launch(ma, mb, mbh, tp, clusters, s);
-  if (kCfgs[cfg].bn == 224) return PairKernel<224, 7, ES>::launch(ma, mb, mbh, tp, clusters, s);
-  return PairKernel<128, 8, ES>::launch(ma, mb, mbh, tp, clusters, s);
+  if (kCfgs[cfg].async_a)
+    return PairKernel<256, 7, ES, true>::launch(ma, mb, mbh, tp, clusters, s);
+  if (kCfgs[cfg].bn == 256) return PairKernel<256, 7, ES, false>::launch(ma, mb, mbh, tp, clusters, s);
+  if (kCfgs[cfg].bn == 224) return PairKernel<224, 7, ES, false>::launch(ma, mb, mbh, tp, clusters, s);
+  return PairKernel<128, 8, ES, false>::launch(ma, mb, mbh, tp, clusters, s);
 }
 
 template <int ES>
@@ -1479,6 +1660,17 @@ mm_status dispatch(int cfg, const CUtensorMap &ma, const CUtensorMap &mb, const 
 }
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// The largest of 16, 8, 4 (else 2, 1) bytes dividing A's base address and its
+// row and batch strides: 16 lets TMA read A, 8 or 4 the cp.async copies.
+int a_piece_bytes(const Problem &p) {
+  const int es = dtype_bytes(p.ta);
+  const uint64_t x = (uint64_t)(uintptr_t)p.A | (uint64_t)(p.lda * es) |
+                     (p.batch > 1 ? (uint64_t)(p.sA * es) : 0ull);
+  for (int g = 16; g > 1; g /= 2)
+    if (x % (uint64_t)g == 0) return g;
+  return 1;
+}
 
 // The main-loop wait limit of the 1-SM kernels (option wait_limit_us; the
 // drain waits keep 2 s, and the 2-SM kernel keeps 2 s throughout).
@@ -1672,13 +1864,20 @@ bool tc_supports(const Problem &p, const DeviceInfo &d, int cfg, std::string *wh
     return no("dimension too large");
   const int es = dtype_bytes(p.ta);
   if (es == 4 && (p.at || !p.bt)) return no("f32 (tf32) needs K-major A and B (layout NT)");
-  if ((uintptr_t)p.A % 16 || (uintptr_t)p.B % 16) return no("A or B not 16-byte aligned");
-  if ((p.lda * es) % 16 || (p.ldb * es) % 16)
-    return no("lda/ldb not a multiple of 16 bytes (TMA stride rule)");
-  if (p.batch > 1) {
-    if (p.sA <= 0 || p.sB <= 0) return no("zero batch stride");
-    if ((p.sA * es) % 16 || (p.sB * es) % 16) return no("batch stride not a multiple of 16 bytes");
+  if (p.batch > 1 && (p.sA <= 0 || p.sB <= 0)) return no("zero batch stride");
+  if (c.async_a) {
+    if (p.at) return no("A must be stored row-major (K-major) for the cp.async copies");
+    if (a_piece_bytes(p) == 16) return no("A is TMA-aligned: the plain configuration applies");
+    if (a_piece_bytes(p) < 4) return no("A rows not 4-byte aligned");
+    if ((p.K * es) % a_piece_bytes(p)) return no("K * element size not a multiple of the copy piece");
+  } else {
+    if ((uintptr_t)p.A % 16) return no("A not 16-byte aligned");
+    if ((p.lda * es) % 16) return no("lda not a multiple of 16 bytes (TMA stride rule)");
+    if (p.batch > 1 && (p.sA * es) % 16) return no("A batch stride not a multiple of 16 bytes");
   }
+  if ((uintptr_t)p.B % 16) return no("B not 16-byte aligned");
+  if ((p.ldb * es) % 16) return no("ldb not a multiple of 16 bytes (TMA stride rule)");
+  if (p.batch > 1 && (p.sB * es) % 16) return no("B batch stride not a multiple of 16 bytes");
   if (p.lda * es >= (1LL << 40) || p.ldb * es >= (1LL << 40) || p.sA * es >= (1LL << 40) ||
       p.sB * es >= (1LL << 40))
     return no("stride too large for TMA");
@@ -1738,17 +1937,21 @@ mm_status launch_tc_impl(const Problem &p, LaunchCtx &ctx, int cfg, bool c_trans
   const int tile_m = c.pair ? 2 * BM : BM;
   CUtensorMap ma, mb;
   mm_status st;
-  // A: logical M x K.  K-major when stored row-major (N), MN-major when T.
-  if (!p.at)
-    st = encode_map(&ma, p.ta, p.A, p.K, p.M, p.batch, p.lda * es, p.sA * es, bk, BM);
-  else
-    st = encode_map(&ma, p.ta, p.A, p.M, p.K, p.batch, p.lda * es, p.sA * es, atom, bk);
-  if (st != MM_OK) return st;
   // B: logical K x N.  K-major when stored transposed (T), MN-major when N.
   if (p.bt)
     st = encode_map(&mb, p.tb, p.B, p.K, p.N, p.batch, p.ldb * es, p.sB * es, bk, bn_cta);
   else
     st = encode_map(&mb, p.tb, p.B, p.N, p.K, p.batch, p.ldb * es, p.sB * es, atom, bk);
+  if (st != MM_OK) return st;
+  // A: logical M x K.  K-major when stored row-major (N), MN-major when T;
+  // copied by cp.async instead where TMA cannot address its rows (the map
+  // argument then only repeats B's)
+  if (c.async_a)
+    ma = mb;
+  else if (!p.at)
+    st = encode_map(&ma, p.ta, p.A, p.K, p.M, p.batch, p.lda * es, p.sA * es, bk, BM);
+  else
+    st = encode_map(&ma, p.ta, p.A, p.M, p.K, p.batch, p.lda * es, p.sA * es, atom, bk);
   if (st != MM_OK) return st;
   // MN-major operands: one 4-D copy per stage instead of one copy per
   // 128-byte-wide box, where the MN extent is a whole number of boxes
@@ -1810,6 +2013,12 @@ mm_status launch_tc_impl(const Problem &p, LaunchCtx &ctx, int cfg, bool c_trans
   tp.err = ctx.dev->d_err;
   tp.timeout_ns = c.pair ? kWaitTimeoutNs : one_sm_wait_limit_ns();
   tp.stall_wait = c.pair ? 0 : get_options().wait_stall;
+  if (c.async_a) {
+    tp.a_ptr = static_cast<const char *>(p.A);
+    tp.a_row_bytes = p.lda * es;
+    tp.a_batch_bytes = p.batch > 1 ? p.sA * es : 0;
+    tp.a_piece = a_piece_bytes(p);
+  }
   tp.a_mn = p.at ? 1 : 0;
   tp.b_mn = p.bt ? 0 : 1;
   const uint32_t fmt = p.ta == MM_F16 ? 0u : p.ta == MM_BF16 ? 1u : 2u;

@@ -104,6 +104,7 @@ def test_every_candidate_runs_somewhere():
         "gemv_t_stream": Case(1, 1000, 704, layout="NT", dist="int4"),
         "tc2_repack_256x256": Case(300, 264, 200, layout="NN", dist="int4", pad=(4, 0, 0)),
         "tc2_repack_256x224": Case(300, 264, 200, layout="NN", dist="int4", pad=(4, 0, 0)),
+        "tc2_cpasync_256x256_s7": Case(300, 264, 200, layout="NN", dist="int4", pad=(4, 0, 0)),
         "tc_repack_128x128": Case(300, 264, 200, layout="TN", dist="int4", pad=(3, 0, 0)),
         "tc_repack_128x64": Case(130, 72, 136, layout="NT", dist="int4", pad=(0, 5, 0)),
         "gemv_swap_tc_repack_splitk_128x64": Case(16, 264, 200, layout="NN", dist="int4",
