@@ -45,9 +45,11 @@ namespace {
 constexpr int BM = 128;
 // 7 warps: A copies, MMA, 4 epilogue warps, B copies
 constexpr int kTcThreads = 224;
-// 2-SM kernel with A copied by cp.async (rows TMA cannot address): 4 more
-// warps (7..10) copy A, warp 0 relays the copies' completion
-constexpr int kTcThreadsAsyncA = 352;
+// 2-SM kernel with A copied by cp.async (rows TMA cannot address): 7 more
+// warps (7..13) copy A, warp 0 relays the copies' completion.  No more copy
+// warps than ring stages (see the copies' loop).
+constexpr int kCopyWarps = 7;
+constexpr int kTcThreadsAsyncA = 224 + 32 * kCopyWarps;
 // 1-SM kernel shared memory after the ring: two 4 KB output staging boxes for
 // each epilogue warp (32 rows x 128 bytes, 128-byte swizzle; also the fallback
 // store path's [32][33] transpose scratch), then the barriers
@@ -848,10 +850,10 @@ __device__ __forceinline__ void fence_proxy_async_all() {
 
 // 128 rows x 128 bytes of A (K block kb of rows m0..m0+127, K-major) into a
 // stage laid out as the 128-byte-swizzled K-major tile the MMA reads (16-byte
-// chunk j of row r at r * 128 + ((j ^ (r % 8)) << 4)).  Thread t of the 128
-// copies piece t % P of rows t / P, t / P + 128 / P, ... (P pieces a row), so
-// a warp reads whole 128-byte row segments.  Rows past M and bytes past K are
-// zero-filled.
+// chunk j of row r at r * 128 + ((j ^ (r % 8)) << 4)), by one warp: lane t
+// copies piece t % P of rows t / P, t / P + 32 / P, ... (P pieces a row), so
+// each copy instruction reads whole 128-byte row segments.  Rows past M and
+// bytes past K are zero-filled.
 template <int BYTES, int ES>
 __device__ __forceinline__ void copy_a_stage(const TcParams &p, uint32_t sa, int m0, int b, int kb,
                                              int t) {
@@ -864,7 +866,7 @@ __device__ __forceinline__ void copy_a_stage(const TcParams &p, uint32_t sa, int
   const char *base = p.a_ptr + (int64_t)b * p.a_batch_bytes + kbyte;
   const uint32_t chunk = (uint32_t)(boff >> 4), half = (uint32_t)(boff & 15);
 #pragma unroll 4
-  for (int r = t / P; r < BM; r += 128 / P) {
+  for (int r = t / P; r < BM; r += 32 / P) {
     const int m = m0 + r;
     const uint32_t valid = m < p.M ? kvalid : 0u;
     const void *src = valid ? base + (int64_t)m * p.a_row_bytes : p.a_ptr;
@@ -1059,7 +1061,7 @@ __global__ void __launch_bounds__(AL ? kTcThreadsAsyncA : kTcThreads, 1)
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full0 + 8 * s, AL ? 3 : 1);  // (AL: the arming and both CTAs' A relays)
       mbar_init(empty0 + 8 * s, 1);  // one commit from the leader
-      if (AL) mbar_init(afull0 + 8 * s, 128);  // each copying thread's cp.async arrival
+      if (AL) mbar_init(afull0 + 8 * s, 32);  // the copying warp's lanes
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull0 + 8 * a, 1);
@@ -1103,8 +1105,8 @@ __global__ void __launch_bounds__(AL ? kTcThreadsAsyncA : kTcThreads, 1)
     // first unit into L2 (whole 16-byte granules inside each row)
     int tm, t0, b, w;
     pair_unit(p, cid, BN, tm, t0, b, w);
-    const int m = tm * PAIR_M + (int)pos * BM + (int)threadIdx.x - 32 * 7;
-    if (m < p.M) {
+    for (int m = tm * PAIR_M + (int)pos * BM + (int)threadIdx.x - 32 * 7;
+         m < min(p.M, tm * PAIR_M + ((int)pos + 1) * BM); m += 32 * kCopyWarps) {
       const uintptr_t row = reinterpret_cast<uintptr_t>(p.a_ptr + (int64_t)b * p.a_batch_bytes +
                                                         (int64_t)m * p.a_row_bytes);
       const int64_t pf = (int64_t)(kPrefetchBytes / STAGE_BYTES) * 128, krow = (int64_t)p.K * ES;
@@ -1253,51 +1255,41 @@ __global__ void __launch_bounds__(AL ? kTcThreadsAsyncA : kTcThreads, 1)
     __syncwarp();
   } else if (AL && warp >= 7) {
     // ------------------------------------------------------------ A copies (both CTAs)
-    // One cp.async group a fill.  Once a fill's group has landed (kLag fills
-    // later, so that about kLag + 1 fills are in flight) the thread fences its
-    // writes to the async proxy and arrives on the stage's afull barrier
-    // (128 arrivals).  kLag < STAGES - 1: issuing fill f + kLag needs only
-    // fill f + kLag - STAGES consumed, which precedes fill f.
-    constexpr int kLag = 3;
-    static_assert(kLag < STAGES - 1, "the copies' lag must stay inside the ring");
-    const int t = (int)threadIdx.x - 32 * 7;
-    int stage = 0;
-    uint32_t phase = 0;
-    bool ok = true;
-    int nfill = 0;
-    for (int u = cid; u < p.total_units && ok; u += ncl) {
+    // Copying warp c takes the fills c, c + kCopyWarps, ... of the ring, one
+    // at a time: it copies the fill, waits for its own copies to land, fences
+    // its writes to the async proxy and arrives (32 lanes) on the stage's
+    // afull barrier.  The fence of a thread orders all of its earlier copies,
+    // so a thread never has a later fill's copies in flight when it fences;
+    // the warps together keep up to a ring's worth of fills in flight.
+    // A parity wait tells only adjacent phases apart: when a warp waits for
+    // the stage of fill f (the consumption of fill f - STAGES), its previous
+    // fill f - kCopyWarps needed the consumption of f - kCopyWarps - STAGES,
+    // which covers fill f - 2 * STAGES only when kCopyWarps <= STAGES; then
+    // the stage's barrier is never two phases behind the one awaited.
+    static_assert(kCopyWarps <= STAGES, "copy warps may not run more than a ring ahead");
+    const int c = warp - 7, t = lane;
+    const int nunits = cid < p.total_units ? (p.total_units - 1 - cid) / ncl + 1 : 0;
+    const int64_t nfills = (int64_t)nunits * p.num_kb;
+    for (int64_t f = c; f < nfills; f += kCopyWarps) {
+      const int stage = (int)(f % STAGES);
+      const uint32_t phase = (uint32_t)(f / STAGES) & 1u;
+      if (!warp_wait(empty0 + 8 * stage, phase ^ 1, abort_flag, p.err, kErrProducer,
+                     p.timeout_ns))
+        break;
       int tm, t0, b, w;
-      pair_unit(p, u, BN, tm, t0, b, w);
-      const int m0 = tm * PAIR_M + (int)pos * BM;
-      for (int kb = 0; kb < p.num_kb; ++kb) {
-        if (!warp_wait(empty0 + 8 * stage, phase ^ 1, abort_flag, p.err, kErrProducer,
-                       p.timeout_ns)) {
-          ok = false;
-          break;
-        }
-        const uint32_t sa = smem_u32(smem + stage * STAGE_BYTES);
-        if (p.a_piece == 8)
-          copy_a_stage<8, ES>(p, sa, m0, b, kb, t);
-        else
-          copy_a_stage<4, ES>(p, sa, m0, b, kb, t);
-        cp_async_commit();
-        if (nfill >= kLag) {
-          cp_async_wait_group<kLag>();
-          fence_proxy_async_all();
-          mbar_arrive(afull0 + 8 * ((nfill - kLag) % STAGES));
-        }
-        ++nfill;
-        if (++stage == STAGES) {
-          stage = 0;
-          phase ^= 1;
-        }
-      }
+      pair_unit(p, cid + (int)(f / p.num_kb) * ncl, BN, tm, t0, b, w);
+      const int m0 = tm * PAIR_M + (int)pos * BM, kb = (int)(f % p.num_kb);
+      const uint32_t sa = smem_u32(smem + stage * STAGE_BYTES);
+      if (p.a_piece == 8)
+        copy_a_stage<8, ES>(p, sa, m0, b, kb, t);
+      else
+        copy_a_stage<4, ES>(p, sa, m0, b, kb, t);
+      cp_async_commit();
+      cp_async_wait_group<0>();
+      fence_proxy_async_all();
+      mbar_arrive(afull0 + 8 * stage);
     }
     cp_async_wait_group<0>();  // no copy in flight when shared memory is released
-    if (ok) {
-      fence_proxy_async_all();
-      for (int f = max(0, nfill - kLag); f < nfill; ++f) mbar_arrive(afull0 + 8 * (f % STAGES));
-    }
   } else {
     // ------------------------------------------------------------ epilogue (both CTAs)
     const int q = warp & 3;
