@@ -62,6 +62,9 @@ for _m in (1, 16, 127, 1000, 4097, 8192):
 
 DEFAULT_WORKLOAD = "square_4096_bf16"
 GEMV_WORKLOAD = "gemv_m1_4096_bf16"
+# configurations whose oracle is also timed on a single core
+SINGLE_THREAD_BASELINE = ("small_256_bf16", "gemv_m1_4096_bf16", "gemv_m8_4096_bf16",
+                          "gemv_m16_4096_bf16")
 
 
 def load_peaks():
@@ -550,10 +553,21 @@ def main():
             import oracle
             oracle.build()
             rate, dt, npts = oracle_rate(A, B, wl, 2.0 if args.report else args.cpu_budget_s)
-            line["cpu_baseline"] = {"value": rate, "unit": "TFLOP/s", "cores": oracle.num_threads(),
+            cores = oracle.num_threads()
+            line["cpu_baseline"] = {"value": rate, "unit": "TFLOP/s", "cores": cores,
                                     "kind": "oracle",
                                     "sample": f"{npts} random output elements (K={wl['K']} each),"
                                               f" {dt:.1f} s"}
+            if name in SINGLE_THREAD_BASELINE and cores > 1:
+                # the small and GEMV configurations are also timed on one core
+                oracle.set_num_threads(1)
+                try:
+                    r1, dt1, n1 = oracle_rate(A, B, wl, 1.0 if args.report else 2.0)
+                finally:
+                    oracle.set_num_threads(cores)
+                line["cpu_baseline_1core"] = {
+                    "value": r1, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+                    "sample": f"{n1} random output elements (K={wl['K']} each), {dt1:.1f} s"}
             print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()

@@ -65,12 +65,19 @@ def _load():
         lib.oracle_round_f16.argtypes = [dp, vp, i64]
         lib.oracle_round_f32.argtypes = [dp, vp, i64]
         lib.oracle_num_threads.restype = ci
+        lib.oracle_set_num_threads.argtypes = [ci]
+        lib.oracle_set_num_threads.restype = None
         _lib = lib
     return _lib
 
 
 def num_threads() -> int:
     return int(_load().oracle_num_threads())
+
+
+def set_num_threads(n: int) -> None:
+    """Threads for the following oracle calls (timing on one core or all)."""
+    _load().oracle_set_num_threads(int(n))
 
 
 def _strides(ld: int, trans: bool):
@@ -143,7 +150,7 @@ def decode(bits_or_vals: np.ndarray, dtype: int) -> np.ndarray:
     raise ValueError(dtype)
 
 
-__all__ = ["build", "gemm_f64", "gemm_points", "round_out", "decode", "num_threads",
+__all__ = ["build", "gemm_f64", "gemm_points", "round_out", "decode", "num_threads", "set_num_threads",
            "key", "bounds", "plan"]
 
 if sys.version_info < (3, 8):  # pragma: no cover

@@ -191,3 +191,13 @@ int oracle_num_threads(void) {
   return 1;
 #endif
 }
+
+/* Use n threads (n >= 1) for the loops above from now on; for timing the
+ * oracle on one core beside all of them.  No effect without OpenMP. */
+void oracle_set_num_threads(int n) {
+#ifdef _OPENMP
+  if (n >= 1) omp_set_num_threads(n);
+#else
+  (void)n;
+#endif
+}

@@ -152,6 +152,28 @@ def test_points_match_full():
     np.testing.assert_array_equal(P, C.reshape(-1))
 
 
+def test_thread_count_changes_nothing():
+    """Each output is one fixed-order fp64 sum, so the oracle's value cannot
+    depend on how many threads share the outputs (one core is timed beside
+    all of them)."""
+    A = synth.make_operand(5, BF16, 37, 300, dist="normal")
+    B = synth.make_operand(6, BF16, 300, 29, dist="normal")
+    full = oracle.num_threads()
+    C = oracle.gemm_f64(A, B, 37, 29, 300)
+    pts = np.array([[0, i, j] for i in range(37) for j in range(29)])
+    P = oracle.gemm_points(A, B, 300, pts)
+    oracle.set_num_threads(1)
+    try:
+        assert oracle.num_threads() == 1 or full == 1
+        C1 = oracle.gemm_f64(A, B, 37, 29, 300)
+        P1 = oracle.gemm_points(A, B, 300, pts)
+    finally:
+        oracle.set_num_threads(full)
+    assert oracle.num_threads() == full
+    np.testing.assert_array_equal(C1, C)
+    np.testing.assert_array_equal(P1, P)
+
+
 def _decode_via_gemm(bits, dtype):
     """Expose the oracle's input decoding through the public gemm: C = A . [1]."""
     A = Op(bits, dtype, 1)
