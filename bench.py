@@ -379,17 +379,11 @@ def run_ours(args, w, name, rank, world, peaks, lite=False):
     ev1 = torch.cuda.Event(enable_timing=True)
     sampler = ClockSampler(dev.index if dev.index is not None else 0)
     if not lite:
-        # the clock sampler polls every 200 ms: keep the same calls running
-        # while it starts, so its record covers this load and the timed
-        # region does not begin on a GPU that has just been idle
+        # the clock sampler (an nvidia-smi process polling every 200 ms) starts
+        # first; the timed region is then a burst, so its denominator is the
+        # burst peak, and the sustained rate is taken separately below
         sampler.start()
-        t_hold = time.perf_counter()
-        i = 0
-        while time.perf_counter() - t_hold < 0.3:
-            for _ in range(50):
-                call(i)
-                i += 1
-            torch.cuda.synchronize()
+        time.sleep(0.3)
     for i in range(args.warmup):
         mm.check(call(i))
     if world > 1:
@@ -405,20 +399,36 @@ def run_ours(args, w, name, rank, world, peaks, lite=False):
     if world > 1:
         torch.distributed.barrier()
     # the sampler polls every 200 ms and a timed region of a few steps is far
-    # shorter: keep the same workload running, untimed, for about half a
-    # second more so that the clock record reflects this load
+    # shorter: keep the same workload running for about a second more so that
+    # the clock record reflects this load; its chunks are timed too, and those
+    # of the second half give the sustained rate (the power cap settles within
+    # a fraction of a second of continuous load)
     t_hold = time.perf_counter()
     i = 0
-    while not lite and time.perf_counter() - t_hold < 0.5:
+    chunks = []
+    while not lite and time.perf_counter() - t_hold < 1.0:
+        c0 = torch.cuda.Event(enable_timing=True)
+        c1 = torch.cuda.Event(enable_timing=True)
+        c0.record(stream)
         for _ in range(50):
             call(i)
             i += 1
+        c1.record(stream)
         torch.cuda.synchronize()
+        chunks.append((time.perf_counter() - t_hold, c0, c1))
     clocks = None
+    sustained = None
     if not lite:
         clocks = sampler.stop()
-        clocks["window"] = ("0.3 s of the same calls before the warm-up, the timed region, and "
-                            "0.5 s of the same calls after it")
+        clocks["window"] = ("0.3 s idle while the sampler starts, the timed region, and 1 s of "
+                            "the same calls after it")
+        late = [c for c in chunks if c[0] >= 0.5]
+        if late:
+            ms = sum(c0.elapsed_time(c1) for _, c0, c1 in late)
+            n_calls = 50 * len(late)
+            sustained = {"ms_per_step": ms / n_calls, "steps": n_calls,
+                         "window": "the second half of 1 s of back-to-back calls after the "
+                                   "timed region (chunks of 50, each timed by events)"}
     total_ms = ev0.elapsed_time(ev1)
     # every warm step is one call of the tuned candidate: its mean device time
     # per launch is the timed loop's device time over the steps
@@ -433,6 +443,9 @@ def run_ours(args, w, name, rank, world, peaks, lite=False):
               for x in sets]
         tB = [x[1].view(tdt).view(K, N) if w["layout"][1] == "N" else x[1].view(tdt).view(N, K).t()
               for x in sets]
+        # timed as the library's burst is: after a 0.3 s pause, 5 warm-up calls
+        torch.cuda.synchronize()
+        time.sleep(0.3)
         for i in range(5):
             torch.matmul(tA[i % R], tB[i % R])
         e0 = torch.cuda.Event(enable_timing=True)
@@ -501,6 +514,17 @@ def run_ours(args, w, name, rank, world, peaks, lite=False):
     }
     if hbm:
         line["gbs"] = nbytes * args.steps * world / (total_ms * 1e-3) / 1e9
+    if sustained is not None:
+        t = sustained["ms_per_step"] * 1e-3
+        if hbm:
+            sustained.update(value=nbytes / t / 1e9, unit="GB/s", peak=peaks["hbm_gbs"],
+                             peak_source=peaks["source"] + " (copy bandwidth)")
+        else:
+            sp = peaks["bf16_tflops_sustained"] * (1.1 / 2.25 if tf32 else 1.0)
+            sustained.update(value=flops / t / 1e12, unit="TFLOP/s", peak=sp,
+                             peak_source=peaks["source"] + " sustained")
+        sustained["frac"] = sustained["value"] / sustained["peak"]
+        line["sustained"] = sustained
     return line, (A, B)
 
 
