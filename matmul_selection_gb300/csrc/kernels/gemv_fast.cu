@@ -306,6 +306,7 @@ constexpr int kStreamU = 4;       // loads in flight a lane, rolled loop
 constexpr int kStreamFixedU = 8;  // loads in flight a lane, unrolled steps
 constexpr int kStreamMaxSteps = 4;
 constexpr int kStreamSegB = 512;  // bytes of a row segment (one warp, 16 bytes a lane)
+constexpr int kStreamCombineMax = 24;  // splits one thread a column adds in the combine
 
 __device__ __forceinline__ float to_f32(float x) { return x; }
 __device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
@@ -423,8 +424,26 @@ __global__ void __launch_bounds__(kStreamThreads, 2) gemv_n_stream_kernel(const 
   if (threadIdx.x == 0) last = atom_add_acq_rel_gpu(g.tickets + tile, 1u) == (unsigned)g.S - 1;
   __syncthreads();
   if (!last) return;
-  // H threads a column: thread h adds the splits [h*S/H, (h+1)*S/H) with all of
-  // their loads in flight, then the H run sums are added in run order.
+  if (g.S <= kStreamCombineMax) {
+    // one thread a column adds the S split sums in split order, all of their
+    // loads in flight (no second exchange through shared memory)
+    if (threadIdx.x < CW) {
+      float x[kStreamCombineMax];
+#pragma unroll
+      for (int q = 0; q < kStreamCombineMax; ++q)
+        x[q] = q < g.S ? __ldcg(ws + (int64_t)q * CW + c) : 0.f;
+      float y = x[0];
+#pragma unroll
+      for (int q = 1; q < kStreamCombineMax; ++q)
+        if (q < g.S) y += x[q];
+      if (col0 + c < g.N) st_any(g.C, (int64_t)b * g.sC + col0 + c, g.tc, y);
+    }
+    if (threadIdx.x == 0) g.tickets[tile] = 0;  // ready for the next call on this stream
+    return;
+  }
+  // more splits: H threads a column, thread h adds the splits
+  // [h*S/H, (h+1)*S/H) with all of their loads in flight, then the H run sums
+  // are added in run order.
   const int h = threadIdx.x / CW;
   const int sb = h * g.S / H, se = (h + 1) * g.S / H;
   float run = 0.f;
