@@ -34,6 +34,11 @@
  * corrupted by tuning.  The library owns its scratch (split-K workspaces,
  * rotating sets, flush buffer) and frees it in mm_shutdown().
  *
+ * Alignment: lhs, rhs and out must each start on a multiple of their element
+ * size (2 bytes for bf16/f16, 4 for f32); a pointer that does not is rejected
+ * with MM_ERR_INVALID_ARG before anything is launched.  Other alignments
+ * (16-byte bases or leading dimensions) only narrow the candidates.
+ *
  * Errors: every entry point returns an mm_status; on failure a thread-local
  * message is available from mm_last_error().  Device pointers are not
  * dereferenced on the host.  Calls are thread-safe; a second caller that

@@ -27,8 +27,8 @@ mm_status mm_tune_key(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
   if (!out) return set_error(MM_ERR_INVALID_ARG, "null key output");
   Problem p;
   // no data pointers are needed for a key: validate with a dummy output
-  static char dummy;
-  mm_status st = make_problem(&p, &dummy, &dummy, &dummy, M, N, K, lda, ldb, ldc, dt, layout, batch);
+  static char dummy[16] __attribute__((aligned(16)));
+  mm_status st = make_problem(&p, dummy, dummy, dummy, M, N, K, lda, ldb, ldc, dt, layout, batch);
   if (st != MM_OK) return st;
   KeyPod k = make_key(p, get_options().level);
   std::memcpy(out->bytes, &k, sizeof k);

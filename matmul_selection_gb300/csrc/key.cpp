@@ -98,6 +98,11 @@ mm_status make_problem(Problem *p, const void *lhs, const void *rhs, void *out, 
   bool empty = (M == 0 || N == 0 || p->batch == 0);
   if (!empty && !out) return set_error(MM_ERR_INVALID_ARG, "null output");
   if (!empty && K > 0 && (!lhs || !rhs)) return set_error(MM_ERR_INVALID_ARG, "null input");
+  // every kernel reads and writes whole elements: an operand must start on a
+  // multiple of its element size
+  if ((uintptr_t)lhs % dtype_bytes(p->ta) || (uintptr_t)rhs % dtype_bytes(p->tb) ||
+      (uintptr_t)out % dtype_bytes(p->tc))
+    return set_error(MM_ERR_INVALID_ARG, "operand pointer not aligned to its element size");
   return MM_OK;
 }
 

@@ -92,6 +92,21 @@ def test_key_batched_matches_oracle():
                                               stride_b=sb)
 
 
+def test_element_misaligned_pointers_rejected_before_any_launch():
+    """An operand that does not start on a multiple of its element size is
+    refused on the host (no kernel can read half an element); the pointers
+    here are never dereferenced, so this runs without a GPU."""
+    bf = (0, 0, 0)
+    f32 = (2, 2, 2)
+    for dt, bad in ((bf, (0x1001, 0x2000, 0x3000)), (bf, (0x1000, 0x2001, 0x3000)),
+                    (bf, (0x1000, 0x2000, 0x3001)), (f32, (0x1002, 0x2000, 0x3000)),
+                    (f32, (0x1000, 0x2000, 0x3006))):
+        for call in (lambda: mm.mm_autotune_execute(*bad, 1, 64, 64, 64, 64, 64, dt, "NT"),
+                     lambda: mm.mm_execute_candidate(0, *bad, 1, 64, 64, 64, 64, 64, dt, "NT")):
+            assert call() == mm.MM_ERR_INVALID_ARG
+            assert "element size" in mm.mm_last_error()
+
+
 def test_key_invalid_arguments():
     assert mm.mm_tune_key(-1, 4, 4, 4, 4, 4, (0, 0, 0), "NN")[0] == mm.MM_ERR_INVALID_ARG
     assert mm.mm_tune_key(4, 4, 4, 3, 4, 4, (0, 0, 0), "NN")[0] == mm.MM_ERR_INVALID_ARG

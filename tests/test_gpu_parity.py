@@ -213,7 +213,10 @@ def test_gemv_t_stream_rows(shape_pad, dt):
     """The transposed-B M=1 GEMV that gives each CTA whole rows of B: fewer
     rows than CTAs, many row blocks a CTA (wide N), K not a multiple of the
     16-byte piece with NaN-filled row padding right after it (elements past K
-    must not reach the sums), three launches in a row over a fresh output."""
+    must not reach the sums), three launches in a row over a fresh output;
+    A read as packed 16-byte pieces (contiguous, aligned, K a whole number of
+    pieces) and element by element (K ragged, batch strides off 16 bytes, A
+    transposed)."""
     shape, pad = shape_pad
     i = NAMES.index("gemv_t_stream")
     c = Case(*shape, layout="NT", dt=dt, dist="int4", pad=(0, pad, 0), seed=sum(shape)).device()
@@ -229,6 +232,16 @@ def test_gemv_t_stream_rows(shape_pad, dt):
     cr = Case(1, 4096, 4096, layout="NT", dt=dt, dist="normal", seed=5).device()
     assert run(i, cr) == mm.MM_OK, mm.mm_last_error()
     cr.check(exact=False)
+    # A stored transposed (its K elements lda apart): A's elements one by one,
+    # at a K that would otherwise take the packed 16-byte pieces of A
+    ct = Case(1, 1000, 704, layout="TT", dt=dt, dist="int4", pad=(3, 0, 0), seed=6).device()
+    assert run(i, ct) == mm.MM_OK, mm.mm_last_error()
+    ct.check(exact=True)
+    # A's base one element off a 16-byte boundary: element by element too
+    ea = 4 if dt[0] == F32 else 2
+    co = Case(1, 1000, 704, layout="NT", dt=dt, dist="int4", a_off=ea, seed=7).device()
+    assert run(i, co) == mm.MM_OK, mm.mm_last_error()
+    co.check(exact=True)
 
 
 @pytest.mark.parametrize("shape", [(1, 4096, 4096), (1, 1000, 700), (1, 136, 5000), (1, 64, 33),
