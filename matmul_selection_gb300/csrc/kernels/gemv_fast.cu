@@ -295,7 +295,7 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1) gemv_n_cluster_kern
 // four steps of kStreamFixedU rows a warp, the step count is a template
 // argument and the loop is unrolled completely, with eight 16-byte loads in
 // flight a lane: straight-line code whose loads the compiler can issue ahead
-// of the previous step's arithmetic (4096 x 4096 bf16: 6.6 us a call against
+// of the previous step's arithmetic (4096 x 4096 bf16: 6.8 us a call against
 // 7.2 us for the rolled loop with four loads in flight, measured back to
 // back).  Deeper splits take the rolled loop.  The S partial sums of a group
 // are combined by whichever of its CTAs finishes last (an atomic ticket), in
