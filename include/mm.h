@@ -248,6 +248,18 @@ int32_t mm_default_candidate(int64_t M, int64_t N, int64_t K, int64_t lda, int64
                              int64_t ldc, mm_dtypes dt, mm_layout layout, const mm_batch *batch);
 
 /*
+ * mm_device_peaks -- the roofline peaks the tuner uses on the current device
+ * (autotune page, section "roofline and the hundred thousand launches": the
+ * probes run once per device): the dense bf16 tensor rate (the peak_tflops
+ * option, else GB300's nominal 2.25 PFLOP/s), the memory bandwidth (the
+ * peak_gbs option, else a timed device copy of 4 x L2 read and written), and
+ * the launch overhead (200 empty launches between two events).  The first
+ * call on a device (or the first tune) runs the probes; later calls return
+ * the cached values.  Null outputs are skipped.  Errors: MM_ERR_CUDA.
+ */
+mm_status mm_device_peaks(double *bf16_ops_per_s, double *bytes_per_s, double *launch_ns);
+
+/*
  * mm_roofline_limit_ns -- the tuning time limit of the autotune page,
  * section "roofline and the hundred thousand launches":
  * max(ops/peak_ops, bytes/peak_bytes) / threshold + launch overhead, in ns.

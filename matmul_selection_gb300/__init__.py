@@ -92,6 +92,7 @@ _sig = {
     "mm_default_candidate": (_i32, [_i64, _i64, _i64, _i64, _i64, _i64, mm_dtypes, ctypes.c_int,
                                     ctypes.POINTER(mm_batch)]),
     "mm_roofline_limit_ns": (ctypes.c_double, [ctypes.c_double] * 6),
+    "mm_device_peaks": (_i32, [ctypes.POINTER(ctypes.c_double)] * 3),
     "mm_set_option": (_i32, [_cp, _cp]),
     "mm_get_option": (_i32, [_cp, ctypes.c_char_p, ctypes.c_size_t]),
     "mm_get_stats": (_i32, [ctypes.POINTER(mm_stats)]),
@@ -266,6 +267,13 @@ def mm_default_candidate(M, N, K, lda, ldb, ldc, dtypes, layout, batch=None):
 def mm_group_name(g):
     r = _lib.mm_group_name(g)
     return r.decode() if r is not None else None
+
+
+def mm_device_peaks():
+    """(status, bf16 ops/s, bytes/s, launch ns) of the current device."""
+    v = [ctypes.c_double(0) for _ in range(3)]
+    st = _lib.mm_device_peaks(*[ctypes.byref(x) for x in v])
+    return (st,) + tuple(x.value for x in v)
 
 
 def mm_roofline_limit_ns(ops, peak_ops_per_s, nbytes, peak_bytes_per_s, threshold, launch_ns):

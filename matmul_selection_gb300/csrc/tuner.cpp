@@ -756,6 +756,23 @@ mm_status autotune_execute(const Problem &p, cudaStream_t s, ExecResult *res) {
 
 }  // namespace mm
 
+extern "C" mm_status mm_device_peaks(double *bf16_ops_per_s, double *bytes_per_s,
+                                     double *launch_ns) {
+  mm::DeviceState *ds = nullptr;
+  mm_status st = mm::current_device(&ds);
+  if (st != MM_OK) return st;
+  mm::Peaks pk;
+  {
+    std::lock_guard<std::mutex> lk(ds->tune_mu);  // the tuner computes them under this lock too
+    st = mm::roofline_peaks(*ds, &pk);
+  }
+  if (st != MM_OK) return st;
+  if (bf16_ops_per_s) *bf16_ops_per_s = pk.bf16_ops;
+  if (bytes_per_s) *bytes_per_s = pk.bytes_per_s;
+  if (launch_ns) *launch_ns = pk.launch_ns;
+  return MM_OK;
+}
+
 extern "C" double mm_roofline_limit_ns(double ops, double peak_ops_per_s, double bytes,
                                        double peak_bytes_per_s, double threshold,
                                        double launch_ns) {

@@ -590,3 +590,16 @@ def test_wait_limit_timeout_is_reported(tmp_path):
         mm.mm_set_option("wait_stall", "0")
         mm.mm_set_option("wait_limit_us", "2000000")
         mm.mm_shutdown()  # drop the inflated peaks
+
+
+def test_device_peaks_probed_once_and_cached():
+    """The roofline peaks (autotune page: probes run once per device): the
+    first query runs or returns the probes, later queries return the same
+    cached values, all positive and plausible for one GB300 (a launch costs
+    well under 100 us; memory and tensor rates above 1 TB/s and 100 TFLOP/s)."""
+    st, ops, bw, launch = mm.mm_device_peaks()
+    assert st == mm.MM_OK, mm.mm_last_error()
+    assert ops > 1e14 and bw > 1e12 and 0 < launch < 1e5
+    again = mm.mm_device_peaks()
+    assert again == (st, ops, bw, launch)
+
