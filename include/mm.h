@@ -130,7 +130,10 @@ mm_status mm_tune_key(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
  * record, then launch the winner on `stream`.  With tuning disabled a miss
  * runs the always-valid default kernel (TunableOp's Default).  M, N or batch
  * of 0 is a no-op; K = 0 writes zeros.  While `stream` is being captured
- * into a CUDA graph a miss is not tuned: the default kernel is captured.
+ * into a CUDA graph a miss is not tuned: the default kernel is captured; a
+ * hit whose recorded winner needs scratch not yet allocated on `stream`
+ * (split-K workspaces, repack copies) captures the next candidate of the
+ * key's ranking that needs none.
  * Errors: MM_ERR_INVALID_ARG, MM_ERR_CUDA, MM_ERR_NO_VALID_CANDIDATE.
  */
 mm_status mm_autotune_execute(const void *lhs, const void *rhs, void *out, int64_t M, int64_t N,

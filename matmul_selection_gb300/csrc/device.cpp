@@ -100,6 +100,14 @@ mm_status get_scratch(DeviceState &ds, cudaStream_t s, int slot, size_t bytes, v
   std::lock_guard<std::mutex> lk(ds.scratch_mu);
   DevBuf &b = ds.scratch[std::make_pair(s, slot)];
   if (!b.ptr || b.bytes < bytes) {
+    // Nothing can be allocated while the stream is being captured into a
+    // graph (the allocation would end the capture): the candidate declines
+    // and the caller moves on to one that needs no new scratch.
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &cap) == cudaSuccess && cap != cudaStreamCaptureStatusNone)
+      return set_error(MM_ERR_UNSUPPORTED,
+                       "scratch of %zu bytes not allocated on this stream before the capture",
+                       bytes);
     // The old buffer may still be read by queued work on this stream.
     if (b.ptr) {
       cudaError_t e = cudaStreamSynchronize(s);

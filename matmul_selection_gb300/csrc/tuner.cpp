@@ -590,8 +590,12 @@ mm_status run_entry(DeviceState &ds, const TableEntry &e, const Problem &p, cuda
     std::string why;
     if (c < 0 || c >= (int)reg.size()) continue;
     if (!reg[c].supports(p, ds.info, reg[c].cfg, &why)) continue;
+    const mm_status st = launch_candidate(c, p, ctx);
+    // a candidate that declines at launch (scratch it cannot allocate while
+    // the stream is captured) leaves the call to the next one in the ranking
+    if (st == MM_ERR_UNSUPPORTED) continue;
     if (res) res->candidate = c;
-    return launch_candidate(c, p, ctx);
+    return st;
   }
   if (res) res->candidate = 0;
   return launch_candidate(0, p, ctx);

@@ -416,6 +416,30 @@ def test_graph_capture_miss_uses_default():
     assert mm.mm_candidate_launches(0) == n0 + 1
 
 
+def test_graph_capture_hit_whose_winner_needs_new_scratch():
+    """A table hit captured on a stream that never ran the recorded winner:
+    split-K needs a workspace on that stream, which cannot be allocated
+    while the stream is captured.  The call must still be captured (the
+    winner declines and the next candidate of the ranking that needs no new
+    scratch runs), and the replayed graph must compute the product."""
+    import torch
+    c = Case(128, 128, 8192, dt=(BF16, BF16, F32), dist="int4", seed=77).device()
+    mm.check(mm.mm_autotune_execute(*c.args()))  # tuned on the default stream
+    torch.cuda.synchronize()
+    _, key, _ = mm.mm_tune_key(128, 128, 8192, c.A.ld, c.B.ld, c.C.ld, (BF16, BF16, F32), "NN")
+    winner = mm.mm_candidate_name(mm.mm_lookup(key)[1])
+    assert "splitk" in winner, f"the case needs a split-K winner, got {winner}"
+    c.dC.fill_(0xFF)
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        st = mm.mm_autotune_execute(*c.args(), stream=s)
+    assert st == 0, mm.mm_last_error()
+    g.replay()
+    torch.cuda.synchronize()
+    c.check(exact=True)
+
+
 # ---------------------------------------------------------------- harness paths
 def _last_decision(path):
     return json.loads(open(path).read().splitlines()[-1])
