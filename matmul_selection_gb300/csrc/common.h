@@ -313,6 +313,10 @@ bool gemv_fast_supports(const Problem &p, const DeviceInfo &d, int cfg, std::str
 mm_status launch_gemv_fast(const Problem &p, LaunchCtx &ctx, int cfg);
 int gemv_fast_config_count();
 const char *gemv_fast_config_name(int cfg);
+bool gemv_mma_supports(const Problem &p, const DeviceInfo &d, int cfg, std::string *why);
+mm_status launch_gemv_mma(const Problem &p, LaunchCtx &ctx, int cfg);
+int gemv_mma_config_count();
+const char *gemv_mma_config_name(int cfg);
 
 bool repack_supports(const Problem &p, const DeviceInfo &d, int cfg, std::string *why);
 mm_status launch_repack(const Problem &p, LaunchCtx &ctx, int cfg);

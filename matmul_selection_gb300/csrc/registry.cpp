@@ -54,6 +54,9 @@ std::vector<Candidate> build_registry() {
   for (int i = 0; i < gemv_fast_config_count(); ++i)
     r.push_back({gemv_fast_config_name(i), GROUP_GEMV, i, prio_gemv, gemv_fast_supports,
                  launch_gemv_fast});
+  for (int i = 0; i < gemv_mma_config_count(); ++i)
+    r.push_back({gemv_mma_config_name(i), GROUP_GEMV, i, prio_gemv, gemv_mma_supports,
+                 launch_gemv_mma});
   for (int i = 0; i < tc_config_count(); ++i)
     r.push_back({tc_config_name(i), GROUP_TENSOR, i, prio_tc, tc_supports, launch_tc});
   for (int i = 0; i < repack_config_count(); ++i) {
@@ -182,8 +185,11 @@ std::vector<PlanItem> make_plan(const KeyPod &k, const Problem &p, const DeviceI
 // the candidate that won that class on a GB300 (the committed tuning table),
 // then the plan's order; the first that supports the problem is taken.
 //   m = 1                  : gemv_n_stream / gemv_t_stream (B row-major / transposed)
-//   m <= 16                : the swapped tensor-core split-K (on a copy of A if
-//                            A's rows are not 16-byte aligned)
+//   m <= 8, B row-major    : gemv_n_mma, then the swapped tensor-core split-K
+//   m <= 16, B row-major,  : gemv_n_mma (it reads such an A in place), then the
+//     A not 16-byte aligned  swapped split-K on a copy of A
+//   m <= 16 otherwise      : the swapped tensor-core split-K (on a copy of A if
+//                            A's rows are not 16-byte aligned), then gemv_n_mma
 //   few tiles, deep k      : split-K (the split-K group rule)
 //   f32 inputs             : tc_128x256_s4, tc_128x128_s6
 //   small outputs          : tc_128x64_s8 (m*n <= 512 x 512: latency)
@@ -194,7 +200,11 @@ std::vector<int> default_order(const KeyPod &k, const Problem &p, const DeviceIn
   if (k.m <= 1) {
     pref = {p.bt ? "gemv_t_stream" : "gemv_n_stream"};
   } else if (k.m <= 16) {
-    pref = {aligned_a ? "gemv_swap_tc_splitk_128x64_s8" : "gemv_swap_tc_repack_splitk_128x64"};
+    const char *swap = aligned_a ? "gemv_swap_tc_splitk_128x64_s8" : "gemv_swap_tc_repack_splitk_128x64";
+    if (!p.bt && (k.m <= 8 || !aligned_a))
+      pref = {"gemv_n_mma", swap};
+    else
+      pref = {swap, "gemv_n_mma"};
   } else if (prio_splitk(k, d) == PRIORITY_HIGH) {
     pref = {aligned_a ? "tc_splitk_128x128_s7" : "tc_repack_splitk_128x128"};
   } else if (p.ta == MM_F32) {

@@ -102,6 +102,7 @@ def test_every_candidate_runs_somewhere():
         "gemv_t_rows": Case(3, 300, 1000, layout="NT", dist="int4"),
         "gemv_n_stream": Case(1, 1000, 700, layout="NN", dist="int4"),
         "gemv_t_stream": Case(1, 1000, 704, layout="NT", dist="int4"),
+        "gemv_n_mma": Case(16, 1000, 520, layout="NN", dt=(BF16, BF16, F32), dist="int4"),
         "tc2_repack_256x256": Case(300, 264, 200, layout="NN", dist="int4", pad=(4, 0, 0)),
         "tc2_repack_256x224": Case(300, 264, 200, layout="NN", dist="int4", pad=(4, 0, 0)),
         "tc2_cpasync_256x256_s7": Case(300, 264, 200, layout="NN", dist="int4", pad=(4, 0, 0)),
@@ -266,6 +267,38 @@ def test_gemv_n_stream_splits(shape, dt):
               pad=(8, 8, 4)).device()
     assert run(i, cb) == mm.MM_OK, mm.mm_last_error()
     cb.check(exact=True)
+
+
+@pytest.mark.parametrize("shape_pad", [((16, 4096, 4096), (0, 0)), ((8, 4096, 4096), (4, 0)),
+                                       ((2, 1000, 700), (0, 0)), ((5, 70, 4100), (0, 2)),
+                                       ((16, 8, 20000), (0, 0)), ((13, 4104, 24), (4, 0)),
+                                       ((16, 264, 1000), (4, 0)), ((3, 1, 17), (3, 7))],
+                         ids=lambda s: "x".join(map(str, s[0])) + "+" + "_".join(map(str, s[1])))
+@pytest.mark.parametrize("dt", [(BF16, BF16, F32), (F16, F16, F16), (BF16, BF16, BF16)],
+                         ids=["bf16-f32", "f16-f16", "bf16-bf16"])
+def test_gemv_n_mma_shapes(shape_pad, dt):
+    """The warp-MMA small-M GEMV: M from 2 to 16 (rows past M zero in the
+    MMA), N ragged against the 64-column groups (including a single column),
+    K ragged against the 16-row chunks and the splits (zero-filled past K),
+    A's leading dimension padded so that its rows are only 8-byte aligned
+    (copied in 8-byte pieces; NaN padding must not reach the sums), B rows
+    padded to 16 bytes, three
+    launches in a row over a fresh output (the arrival counters back at
+    zero), a batch with gaps, and a real-valued case."""
+    shape, (pa, pb) = shape_pad
+    i = NAMES.index("gemv_n_mma")
+    c = Case(*shape, layout="NN", dt=dt, dist="int4", pad=(pa, pb, 0), seed=sum(shape)).device()
+    for _ in range(3):
+        c.device()
+        assert run(i, c) == mm.MM_OK, mm.mm_last_error()
+        c.check(exact=True)
+    cb = Case(7, 296, 900, layout="NN", dt=dt, dist="int4", batch=3, bstride_extra=(8, 16, 8),
+              pad=(4, 8, 4)).device()
+    assert run(i, cb) == mm.MM_OK, mm.mm_last_error()
+    cb.check(exact=True)
+    cr = Case(16, 4096, 4096, layout="NN", dt=dt, dist="normal", seed=9).device()
+    assert run(i, cr) == mm.MM_OK, mm.mm_last_error()
+    cr.check(exact=False)
 
 
 @pytest.mark.parametrize("shape", [(1, 4096, 4096), (3, 37, 4104), (8, 64, 2056), (2, 20, 104),
