@@ -52,6 +52,7 @@ struct MmaArgs {
   int64_t ldc, sC;
   int M, N, K, batch;
   int G, S;           // column groups, K splits (in whole 16-row chunks)
+  int cq, crem;       // chunks / S and chunks % S: split sp has chunks [sp*cq + min(sp, crem), + cq + (sp < crem))
   float *ws;          // [batch][G][S][16][64] split sums
   unsigned *tickets;  // [batch][G] arrival counters, zero between calls
 };
@@ -125,8 +126,9 @@ __device__ __forceinline__ int clampi(int v, int lo, int hi) { return v < lo ? l
 // loop is unrolled STEPS times (a trip count the compiler can see lets it
 // schedule the copies and MMAs of consecutive chunks together: 9.96 against
 // 10.40 us a call at M = 16, 4096 x 4096, measured back to back); STEPS = 0:
-// a loop.
-template <int TT, int XP, int STEPS>
+// a loop.  EVEN: every warp has exactly STEPS chunks, all inside K and every
+// group inside N (the host checks), so no copy needs a bound.
+template <int TT, int XP, int STEPS, bool EVEN>
 __global__ void __launch_bounds__(kMmaThreads, 2) gemv_n_mma_kernel(const MmaArgs g) {
   pdl_launch_dependents();
   constexpr int NB = kMmaCW / 8;  // 8-column blocks of a group
@@ -134,24 +136,24 @@ __global__ void __launch_bounds__(kMmaThreads, 2) gemv_n_mma_kernel(const MmaArg
   __shared__ unsigned last;
   const int b = blockIdx.y;
   const int grp = blockIdx.x / g.S, sp = blockIdx.x - grp * g.S;
-  const int nch = (g.K + 15) / 16;
-  const int c0 = (int)((int64_t)sp * nch / g.S), c1 = (int)((int64_t)(sp + 1) * nch / g.S);
+  // the first crem splits take one chunk more (no division before the prefetch)
+  const int c0 = sp * g.cq + min(sp, g.crem), c1 = c0 + g.cq + (sp < g.crem ? 1 : 0);
   const int col0 = grp * kMmaCW;
   const char *Bb = g.B + (int64_t)b * g.sB * 2;
   const char *Ab = g.A + (int64_t)b * g.sA * 2;
   {  // this CTA's rows of B (whole 16-byte pieces of its columns) into L2 before the wait
-    const int run = (clampi(g.N - col0, 0, kMmaCW) * 2) & ~15;
-    const int r1 = c1 * 16 < g.K ? c1 * 16 : g.K;
+    const int run = EVEN ? kMmaRowB : (clampi(g.N - col0, 0, kMmaCW) * 2) & ~15;
+    const int r1 = EVEN || c1 * 16 < g.K ? c1 * 16 : g.K;
     if (run > 0)
       for (int r = c0 * 16 + (int)threadIdx.x; r < r1; r += kMmaThreads)
         prefetch_l2(Bb + ((int64_t)r * g.ldb + col0) * 2, (uint32_t)run);
   }
   pdl_wait();  // A, the workspace, the tickets and C only after the previous kernel
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int mine = c1 - c0 > warp ? (c1 - c0 - warp + kMmaWarps - 1) / kMmaWarps : 0;
+  const int mine = EVEN ? STEPS : c1 - c0 > warp ? (c1 - c0 - warp + kMmaWarps - 1) / kMmaWarps : 0;
   uint8_t *wbase = dsm + (size_t)warp * kMmaStages * kMmaStageB;
   // a group wholly inside N over whole 16-row chunks copies B unchecked
-  const bool b_whole = col0 + kMmaCW <= g.N && g.K % 16 == 0;
+  const bool b_whole = EVEN || (col0 + kMmaCW <= g.N && g.K % 16 == 0);
   // copies of the warp's i-th chunk into stage i % kMmaStages (an empty group
   // past the last chunk keeps the wait counts uniform)
   auto issue = [&](int i) {
@@ -177,26 +179,43 @@ __global__ void __launch_bounds__(kMmaThreads, 2) gemv_n_mma_kernel(const MmaArg
           cp16(dst + row * kMmaRowB + ((piece ^ (row & 7)) << 4), src, (uint32_t)valid);
         }
       }
-      // A: 16 rows x 32 bytes (k = 16c .. 16c + 15), rows past M and k past K zero
+      // A: rows below M of the 16 x 32-byte tile (k = 16c .. 16c + 15), k
+      // past K zero; the rows from M on were cleared once
       const int k0 = c * 16;
       if constexpr (XP == 16) {
         const int m = lane >> 1, h = lane & 1;
-        const int valid = m < g.M ? clampi(g.K - (k0 + 8 * h), 0, 8) * 2 : 0;
-        const char *src = valid ? Ab + ((int64_t)m * g.lda + k0 + 8 * h) * 2 : g.A;
-        cp16(dst + 16 * kMmaRowB + m * 32 + ((h ^ ((m >> 2) & 1)) << 4), src, (uint32_t)valid);
+        if (m < g.M) {
+          const int valid = EVEN ? 16 : clampi(g.K - (k0 + 8 * h), 0, 8) * 2;
+          const char *src = valid ? Ab + ((int64_t)m * g.lda + k0 + 8 * h) * 2 : g.A;
+          cp16(dst + 16 * kMmaRowB + m * 32 + ((h ^ ((m >> 2) & 1)) << 4), src, (uint32_t)valid);
+        }
       } else {
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
           const int e = lane + 32 * j, m = e >> 2, q = e & 3, h = q >> 1;
-          const int valid = m < g.M ? clampi(g.K - (k0 + 4 * q), 0, 4) * 2 : 0;
-          const char *src = valid ? Ab + ((int64_t)m * g.lda + k0 + 4 * q) * 2 : g.A;
-          cp8(dst + 16 * kMmaRowB + m * 32 + ((h ^ ((m >> 2) & 1)) << 4) + (q & 1) * 8, src,
-              (uint32_t)valid);
+          if (m < g.M) {
+            const int valid = EVEN ? 8 : clampi(g.K - (k0 + 4 * q), 0, 4) * 2;
+            const char *src = valid ? Ab + ((int64_t)m * g.lda + k0 + 4 * q) * 2 : g.A;
+            cp8(dst + 16 * kMmaRowB + m * 32 + ((h ^ ((m >> 2) & 1)) << 4) + (q & 1) * 8, src,
+                (uint32_t)valid);
+          }
         }
       }
     }
     cp_commit();
   };
+  // A's rows from M on (the MMA's rows past the problem) zero in every stage,
+  // cleared once here and never copied: 32 bytes a row, whatever the swizzle
+  if (g.M < 16) {
+#pragma unroll
+    for (int st = 0; st < kMmaStages; ++st) {
+      const int m = lane >> 1;
+      if (m >= g.M)
+        *reinterpret_cast<uint4 *>(wbase + (size_t)st * kMmaStageB + 16 * kMmaRowB + lane * 16) =
+            make_uint4(0u, 0u, 0u, 0u);
+    }
+    __syncwarp();  // ordered before any lane's fragment loads
+  }
 #pragma unroll
   for (int i = 0; i < kMmaStages - 1; ++i) issue(i);
   float acc[NB][4];
@@ -275,7 +294,7 @@ __global__ void __launch_bounds__(kMmaThreads, 2) gemv_n_mma_kernel(const MmaArg
   }
   auto store = [&](int o, float v) {
     const int m = o / kMmaCW, n = col0 + o % kMmaCW;
-    if (m < g.M && n < g.N) store_out(g.C, g.tc, (int64_t)b * g.sC + (int64_t)m * g.ldc + n, v);
+    if (m < g.M && (EVEN || n < g.N)) store_out(g.C, g.tc, (int64_t)b * g.sC + (int64_t)m * g.ldc + n, v);
   };
   if (g.S == 1) {
 #pragma unroll
@@ -328,9 +347,9 @@ int mma_steps(const MmaArgs &g) {
   return per_warp <= 2 ? 2 : per_warp <= 4 ? 4 : per_warp <= 8 ? 8 : per_warp <= 16 ? 16 : 0;
 }
 
-template <int TT, int XP, int STEPS>
+template <int TT, int XP, int STEPS, bool EVEN = false>
 mm_status launch_mma(const MmaArgs &g, cudaStream_t s) {
-  auto kern = gemv_n_mma_kernel<TT, XP, STEPS>;
+  auto kern = gemv_n_mma_kernel<TT, XP, STEPS, EVEN>;
   static std::once_flag once;
   static cudaError_t attr = cudaSuccess;
   std::call_once(once, [&] {
@@ -344,6 +363,15 @@ mm_status launch_mma(const MmaArgs &g, cudaStream_t s) {
 
 template <int TT, int XP>
 mm_status launch_steps(const MmaArgs &g, cudaStream_t s) {
+  // every split kMmaWarps * steps whole chunks, every group whole
+  const bool even = g.N % kMmaCW == 0 && g.K % 16 == 0 && g.crem == 0 && g.cq % kMmaWarps == 0;
+  if (even) switch (g.cq / kMmaWarps) {
+    case 2: return launch_mma<TT, XP, 2, true>(g, s);
+    case 4: return launch_mma<TT, XP, 4, true>(g, s);
+    case 8: return launch_mma<TT, XP, 8, true>(g, s);
+    case 16: return launch_mma<TT, XP, 16, true>(g, s);
+    default: break;
+    }
   switch (mma_steps(g)) {
   case 2: return launch_mma<TT, XP, 2>(g, s);
   case 4: return launch_mma<TT, XP, 4>(g, s);
@@ -398,6 +426,9 @@ mm_status launch_gemv_mma(const Problem &p, LaunchCtx &ctx, int cfg) {
   g.K = (int)p.K;
   g.batch = (int)p.batch;
   mma_plan(p.N, p.K, p.batch, ctx.dev->info.sms, &g.G, &g.S);
+  const int nch = (g.K + 15) / 16;
+  g.cq = nch / g.S;
+  g.crem = nch % g.S;
   if (g.S > 1) {
     const size_t ws_bytes = (size_t)p.batch * g.G * g.S * 16 * kMmaCW * sizeof(float);
     const size_t tickets_bytes = (size_t)p.batch * g.G * sizeof(unsigned);

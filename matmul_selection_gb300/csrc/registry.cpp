@@ -185,11 +185,10 @@ std::vector<PlanItem> make_plan(const KeyPod &k, const Problem &p, const DeviceI
 // the candidate that won that class on a GB300 (the committed tuning table),
 // then the plan's order; the first that supports the problem is taken.
 //   m = 1                  : gemv_n_stream / gemv_t_stream (B row-major / transposed)
-//   m <= 8, B row-major    : gemv_n_mma, then the swapped tensor-core split-K
-//   m <= 16, B row-major,  : gemv_n_mma (it reads such an A in place), then the
-//     A not 16-byte aligned  swapped split-K on a copy of A
+//   m <= 16, A and B       : gemv_n_mma (it also reads an A whose rows are only
+//     row-major              8-byte aligned in place)
 //   m <= 16 otherwise      : the swapped tensor-core split-K (on a copy of A if
-//                            A's rows are not 16-byte aligned), then gemv_n_mma
+//                            A's rows are not 16-byte aligned)
 //   few tiles, deep k      : split-K (the split-K group rule)
 //   f32 inputs             : tc_128x256_s4, tc_128x128_s6
 //   small outputs          : tc_128x64_s8 (m*n <= 512 x 512: latency)
@@ -201,10 +200,7 @@ std::vector<int> default_order(const KeyPod &k, const Problem &p, const DeviceIn
     pref = {p.bt ? "gemv_t_stream" : "gemv_n_stream"};
   } else if (k.m <= 16) {
     const char *swap = aligned_a ? "gemv_swap_tc_splitk_128x64_s8" : "gemv_swap_tc_repack_splitk_128x64";
-    if (!p.bt && (k.m <= 8 || !aligned_a))
-      pref = {"gemv_n_mma", swap};
-    else
-      pref = {swap, "gemv_n_mma"};
+    pref = {"gemv_n_mma", swap};  // the first supports only row-major A and B
   } else if (prio_splitk(k, d) == PRIORITY_HIGH) {
     pref = {aligned_a ? "tc_splitk_128x128_s7" : "tc_repack_splitk_128x128"};
   } else if (p.ta == MM_F32) {

@@ -301,6 +301,27 @@ def test_gemv_n_mma_shapes(shape_pad, dt):
     cr.check(exact=False)
 
 
+@pytest.mark.parametrize("shape_pad_batch", [((4, 128, 4096), (0, 0), 1), ((6, 1216, 8192), (4, 8), 1),
+                                             ((3, 8192, 4096), (0, 0), 1), ((5, 256, 4096), (4, 0), 2)],
+                         ids=lambda s: "x".join(map(str, s[0])) + "+" + "_".join(map(str, s[1])) +
+                         f"+b{s[2]}")
+@pytest.mark.parametrize("dt", [(BF16, BF16, F32), (F16, F16, F16)], ids=["bf16-f32", "f16-f16"])
+def test_gemv_n_mma_even_splits(shape_pad_batch, dt):
+    """Shapes whose K splits give every warp the same whole number of 16-row
+    chunks and whose N is a whole number of 64-column groups, so the kernel
+    runs its unchecked instance: with 152 SMs these take 2, 4, 16 and (with a
+    batch of two) 2 chunks a warp; A padded to 8-byte rows in two of them."""
+    shape, (pa, pb), batch = shape_pad_batch
+    i = NAMES.index("gemv_n_mma")
+    extra = (8, 16, 8) if batch > 1 else (0, 0, 0)
+    c = Case(*shape, layout="NN", dt=dt, dist="int4", pad=(pa, pb, 0), batch=batch,
+             bstride_extra=extra, seed=sum(shape) + batch).device()
+    for _ in range(2):
+        c.device()
+        assert run(i, c) == mm.MM_OK, mm.mm_last_error()
+        c.check(exact=True)
+
+
 @pytest.mark.parametrize("shape", [(1, 4096, 4096), (3, 37, 4104), (8, 64, 2056), (2, 20, 104),
                                    (1, 17, 8)], ids=lambda s: "x".join(map(str, s)))
 @pytest.mark.parametrize("dt", [(BF16, BF16, BF16), (F32, F32, F32)], ids=["bf16", "f32"])

@@ -181,7 +181,7 @@ def test_tuning_disabled_runs_default():
 @pytest.mark.parametrize("shape,layout,pad,dt,batch,want", [
     ((1, 4096, 4096), "NN", 0, (BF16, BF16, BF16), None, "gemv_n_stream"),
     ((1, 4096, 4096), "NT", 0, (BF16, BF16, BF16), None, "gemv_t_stream"),
-    ((16, 4096, 4096), "NN", 0, (BF16, BF16, BF16), None, "gemv_swap_tc_splitk_128x64_s8"),
+    ((16, 4096, 4096), "NN", 0, (BF16, BF16, BF16), None, "gemv_n_mma"),
     ((16, 4096, 4096), "NN", 4, (BF16, BF16, BF16), None, "gemv_n_mma"),
     ((8, 4096, 4096), "NN", 0, (BF16, BF16, BF16), None, "gemv_n_mma"),
     ((8, 4096, 4096), "NT", 0, (BF16, BF16, BF16), None, "gemv_swap_tc_splitk_128x64_s8"),
