@@ -1,6 +1,7 @@
 // Internal declarations of the GB300 autotuned matmul library.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <atomic>
@@ -35,7 +36,28 @@ __device__ __forceinline__ void pdl_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// L2 prefetch of one box of a tensor map (element coordinates x, y, z).  It
+// writes no shared memory and returns nothing to the SM, so it may run before
+// pdl_wait(): the data it warms is read after the wait, through the coherent
+// L2.  The innermost coordinate x must be a multiple of 16 bytes; boxes that
+// reach past the tensor are clipped.
+__device__ __forceinline__ void prefetch_box_l2(const CUtensorMap *map, int x, int y, int z) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y), "r"(z)
+               : "memory");
+}
 #endif
+
+// A tensor map over a row-major operand -- `inner` elements a row (stride
+// ld_bytes), `outer` rows, `batch` matrices bstride_bytes apart -- used only
+// for L2 prefetch boxes of box_inner x box_outer elements (no swizzle: the
+// box's row is any multiple of 16 bytes; both extents at most 256).  Needs a
+// 16-byte aligned base and strides that are multiples of 16 bytes.
+mm_status encode_prefetch_map(CUtensorMap *map, int dtype, const void *base, uint64_t inner,
+                              uint64_t outer, uint64_t batch, uint64_t ld_bytes,
+                              uint64_t bstride_bytes, uint32_t box_inner, uint32_t box_outer);
 
 // Launch `kern` with the programmatic-serialization attribute and, unless
 // `cluster` is 1 x 1 x 1, that cluster shape.

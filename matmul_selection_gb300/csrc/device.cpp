@@ -1,4 +1,6 @@
 // Per-device state: properties, error word, private tuning stream, scratch.
+#include <cudaTypedefs.h>
+
 #include <cstdio>
 
 #include "common.h"
@@ -120,6 +122,36 @@ mm_status get_scratch(DeviceState &ds, cudaStream_t s, int slot, size_t bytes, v
     if (e != cudaSuccess) return cuda_error(e, "cudaMemsetAsync (scratch)");
   }
   *out = b.ptr;
+  return MM_OK;
+}
+
+mm_status encode_prefetch_map(CUtensorMap *map, int dtype, const void *base, uint64_t inner,
+                              uint64_t outer, uint64_t batch, uint64_t ld_bytes,
+                              uint64_t bstride_bytes, uint32_t box_inner, uint32_t box_outer) {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  if (!fn) return set_error(MM_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
+  if (batch <= 1) bstride_bytes = ((ld_bytes * outer) + 15) & ~(uint64_t)15;
+  const CUtensorMapDataType t = dtype == MM_BF16  ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                : dtype == MM_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                  : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+  cuuint64_t dims[3] = {inner, outer, batch < 1 ? 1 : batch};
+  cuuint64_t strides[2] = {ld_bytes, bstride_bytes};
+  cuuint32_t box[3] = {box_inner, box_outer, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, t, 3, const_cast<void *>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return set_error(MM_ERR_CUDA, "cuTensorMapEncodeTiled (prefetch map) failed (%d)", (int)r);
   return MM_OK;
 }
 
