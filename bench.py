@@ -264,7 +264,7 @@ def kernel_sources(kernel_name):
         names = ["tc_gemm.cu"]
     elif kernel_name in ("gemv_n_cluster", "gemv_t_rows", "gemv_n_stream", "gemv_t_stream"):
         names = ["gemv_fast.cu"]
-    elif kernel_name == "gemv_n_mma":
+    elif kernel_name in ("gemv_n_mma", "gemv_t_mma"):
         names = ["gemv_mma.cu"]
     elif kernel_name.startswith("gemv"):
         names = ["gemv.cu"]

@@ -240,7 +240,8 @@ const char *mm_group_name(int32_t group);
  * current device (tuning off, or a pending key whose tuner did not finish in
  * time; the TunableOp guide's Default, made a heuristic): a shape-class
  * preference drawn from the GB300 tuning results (M = 1: the streaming
- * GEMVs; M <= 16: the warp-MMA GEMV for A and B row-major, else the swapped
+ * GEMVs; M <= 16: the warp-MMA GEMV for A and B row-major, or for B
+ * transposed when A's rows are not 16-byte aligned, else the swapped
  * tensor-core split-K; few tiles and deep K:
  * split-K; f32: the 1-SM tile; small outputs: the 128 x 64 tile; otherwise
  * the 2-SM 256 x 256 tile, or the copying form when A's rows are not 16-byte

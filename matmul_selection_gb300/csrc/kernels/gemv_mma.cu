@@ -19,6 +19,14 @@
 //       Before its grid dependency wait each CTA prefetches its rows of B
 //       into L2, a few tensor-map boxes a CTA.
 //
+//   gemv_t_mma  the same with B transposed (stored [N][K], each output
+//       column a contiguous row of B): a chunk of B is then 64 rows of n x 32
+//       bytes of k, stored in shared memory as 32-byte rows with the two
+//       16-byte halves swapped on every other group of four rows (as A's
+//       tile), and read by plain ldmatrix, whose 8 x 8 matrices of (n, k)
+//       are exactly the MMA's "col" fragments of B.  Everything else is
+//       shared; B's L2 boxes are 256 k x 8 rows.
+//
 // A need not be 16-byte aligned: its chunks are copied in 8-byte pieces when
 // its base or leading dimension is only 8-byte aligned (lda = 4100 bf16, for
 // instance), so a misaligned A needs no copy of its own.
@@ -109,6 +117,8 @@ __device__ __forceinline__ unsigned atom_add_acq_rel(unsigned *p) {
   return old;
 }
 constexpr int kPfRows = 32;  // rows of B an L2 prefetch box covers (a group wide, 4 KB)
+constexpr int kPfTK = 256;   // B transposed: a box is 256 k x 8 rows of n (4 KB)
+constexpr int kPfTN = 8;
 __device__ __forceinline__ void store_out(void *C, int tc, int64_t i, float v) {
   if (tc == MM_F32)
     static_cast<float *>(C)[i] = v;
@@ -125,10 +135,11 @@ __device__ __forceinline__ int clampi(int v, int lo, int hi) { return v < lo ? l
 // schedule the copies and MMAs of consecutive chunks together: 9.96 against
 // 10.40 us a call at M = 16, 4096 x 4096, measured back to back); STEPS = 0:
 // a loop.  EVEN: every warp has exactly STEPS chunks, all inside K and every
-// group inside N (the host checks), so no copy needs a bound.
-template <int TT, int XP, int STEPS, bool EVEN>
+// group inside N (the host checks), so no copy needs a bound.  BT: B is
+// stored transposed ([N][K]).
+template <int TT, int XP, int STEPS, bool EVEN, bool BT>
 __global__ void __launch_bounds__(kMmaThreads, 2)
-    gemv_n_mma_kernel(const MmaArgs g, const __grid_constant__ CUtensorMap tmB) {
+    gemv_mma_kernel(const MmaArgs g, const __grid_constant__ CUtensorMap tmB) {
   pdl_launch_dependents();
   constexpr int NB = kMmaCW / 8;  // 8-column blocks of a group
   extern __shared__ __align__(128) uint8_t dsm[];
@@ -146,9 +157,16 @@ __global__ void __launch_bounds__(kMmaThreads, 2)
      // 9.81 / 9.99; boxes of 256 rows 9.38 / 9.70 / 9.79, 128 rows 9.36 /
      // 9.66 / 9.79, 64 rows 9.31 / 9.65 / 9.68, 32 rows 9.29 / 9.62 / 9.64,
      // 16 rows 9.29 / 9.65 / 9.66
-    const int r0 = c0 * 16, nbox = ((c1 - c0) * 16 + kPfRows - 1) / kPfRows;
-    for (int t = (int)threadIdx.x; t < nbox; t += kMmaThreads)
-      prefetch_box_l2(&tmB, col0, r0 + t * kPfRows, b);
+    const int r0 = c0 * 16;
+    if constexpr (BT) {  // rows col0 .. col0 + 63 of B's [N][K], k from r0
+      const int nbox = ((c1 - c0) * 16 + kPfTK - 1) / kPfTK * (kMmaCW / kPfTN);
+      for (int t = (int)threadIdx.x; t < nbox; t += kMmaThreads)
+        prefetch_box_l2(&tmB, r0 + (t / (kMmaCW / kPfTN)) * kPfTK, col0 + (t % (kMmaCW / kPfTN)) * kPfTN, b);
+    } else {
+      const int nbox = ((c1 - c0) * 16 + kPfRows - 1) / kPfRows;
+      for (int t = (int)threadIdx.x; t < nbox; t += kMmaThreads)
+        prefetch_box_l2(&tmB, col0, r0 + t * kPfRows, b);
+    }
   }
   pdl_wait();  // A, the workspace, the tickets and C only after the previous kernel
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -162,8 +180,23 @@ __global__ void __launch_bounds__(kMmaThreads, 2)
     if (i < mine) {
       const int c = c0 + warp + i * kMmaWarps;
       const uint32_t dst = smem_addr(wbase + (size_t)(i % kMmaStages) * kMmaStageB);
-      // B: 16 rows x 8 pieces; lane: pieces lane % 8 of rows lane / 8 + 4 j
-      if (b_whole) {
+      if constexpr (BT) {
+        // B: 64 rows of n x 2 pieces (k 16c .. 16c + 7, + 8 .. + 15); lane:
+        // piece lane % 2 of rows lane / 2 + 16 j
+        const int k = c * 16 + (lane & 1) * 8;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int row = (lane >> 1) + 16 * j, h = lane & 1, n = col0 + row;
+          const uint32_t d = dst + row * 32 + ((h ^ ((row >> 2) & 1)) << 4);
+          if (b_whole) {
+            cp16(d, Bb + ((int64_t)n * g.ldb + k) * 2, 16u);
+          } else {
+            const int valid = n < g.N ? clampi(g.K - k, 0, 8) * 2 : 0;
+            cp16(d, valid ? Bb + ((int64_t)n * g.ldb + k) * 2 : g.B, (uint32_t)valid);
+          }
+        }
+      } else if (b_whole) {
+        // B: 16 rows x 8 pieces; lane: pieces lane % 8 of rows lane / 8 + 4 j
         const char *src = Bb + ((int64_t)(c * 16 + lane / 8) * g.ldb + col0 + (lane % 8) * 8) * 2;
         const int64_t step4 = 4 * g.ldb * 2;
 #pragma unroll
@@ -240,9 +273,14 @@ __global__ void __launch_bounds__(kMmaThreads, 2)
 #pragma unroll
     for (int nb = 0; nb < NB; nb += 2) {
       const int mat = lane >> 3, r = lane & 7;
-      const int krow = (mat & 1) * 8 + r, piece = nb + (mat >> 1);
       uint32_t b0, b1, b2, b3;
-      ldm_x4_trans(base + krow * kMmaRowB + ((piece ^ (krow & 7)) << 4), b0, b1, b2, b3);
+      if constexpr (BT) {  // rows of n, 8 k a matrix row: no transpose
+        const int nrow = (nb + (mat >> 1)) * 8 + r, h = mat & 1;
+        ldm_x4(base + nrow * 32 + ((h ^ ((nrow >> 2) & 1)) << 4), b0, b1, b2, b3);
+      } else {
+        const int krow = (mat & 1) * 8 + r, piece = nb + (mat >> 1);
+        ldm_x4_trans(base + krow * kMmaRowB + ((piece ^ (krow & 7)) << 4), b0, b1, b2, b3);
+      }
       mma_16816<TT>(acc[nb], a, b0, b1);
       mma_16816<TT>(acc[nb + 1], a, b2, b3);
     }
@@ -349,58 +387,68 @@ int mma_steps(const MmaArgs &g) {
   return per_warp <= 2 ? 2 : per_warp <= 4 ? 4 : per_warp <= 8 ? 8 : per_warp <= 16 ? 16 : 0;
 }
 
-template <int TT, int XP, int STEPS, bool EVEN = false>
+template <bool BT, int TT, int XP, int STEPS, bool EVEN = false>
 mm_status launch_mma(const MmaArgs &g, const CUtensorMap &tm, cudaStream_t s) {
-  auto kern = gemv_n_mma_kernel<TT, XP, STEPS, EVEN>;
+  auto kern = gemv_mma_kernel<TT, XP, STEPS, EVEN, BT>;
   static std::once_flag once;
   static cudaError_t attr = cudaSuccess;
   std::call_once(once, [&] {
     attr = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kMmaSmem);
   });
-  if (attr != cudaSuccess) return cuda_error(attr, "gemv_n_mma shared memory attribute");
+  if (attr != cudaSuccess) return cuda_error(attr, "gemv_mma shared memory attribute");
   cudaError_t e = launch_pdl(kern, dim3((unsigned)(g.G * g.S), (unsigned)g.batch),
                              dim3(kMmaThreads), kMmaSmem, s, dim3(1), g, tm);
-  return e == cudaSuccess ? MM_OK : cuda_error(e, "gemv_n_mma launch");
+  return e == cudaSuccess ? MM_OK : cuda_error(e, "gemv_mma launch");
 }
 
-template <int TT, int XP>
+template <bool BT, int TT, int XP>
 mm_status launch_steps(const MmaArgs &g, const CUtensorMap &tm, cudaStream_t s) {
   // every split kMmaWarps * steps whole chunks, every group whole
   const bool even = g.N % kMmaCW == 0 && g.K % 16 == 0 && g.crem == 0 && g.cq % kMmaWarps == 0;
   if (even) switch (g.cq / kMmaWarps) {
-    case 2: return launch_mma<TT, XP, 2, true>(g, tm, s);
-    case 4: return launch_mma<TT, XP, 4, true>(g, tm, s);
-    case 8: return launch_mma<TT, XP, 8, true>(g, tm, s);
-    case 16: return launch_mma<TT, XP, 16, true>(g, tm, s);
+    case 2: return launch_mma<BT, TT, XP, 2, true>(g, tm, s);
+    case 4: return launch_mma<BT, TT, XP, 4, true>(g, tm, s);
+    case 8: return launch_mma<BT, TT, XP, 8, true>(g, tm, s);
+    case 16: return launch_mma<BT, TT, XP, 16, true>(g, tm, s);
     default: break;
     }
   switch (mma_steps(g)) {
-  case 2: return launch_mma<TT, XP, 2>(g, tm, s);
-  case 4: return launch_mma<TT, XP, 4>(g, tm, s);
-  case 8: return launch_mma<TT, XP, 8>(g, tm, s);
-  case 16: return launch_mma<TT, XP, 16>(g, tm, s);
-  default: return launch_mma<TT, XP, 0>(g, tm, s);
+  case 2: return launch_mma<BT, TT, XP, 2>(g, tm, s);
+  case 4: return launch_mma<BT, TT, XP, 4>(g, tm, s);
+  case 8: return launch_mma<BT, TT, XP, 8>(g, tm, s);
+  case 16: return launch_mma<BT, TT, XP, 16>(g, tm, s);
+  default: return launch_mma<BT, TT, XP, 0>(g, tm, s);
   }
 }
 
+template <bool BT>
+mm_status launch_types(const MmaArgs &g, const CUtensorMap &tm, int ta, bool x16, cudaStream_t s) {
+  if (ta == MM_BF16)
+    return x16 ? launch_steps<BT, MM_BF16, 16>(g, tm, s) : launch_steps<BT, MM_BF16, 8>(g, tm, s);
+  return x16 ? launch_steps<BT, MM_F16, 16>(g, tm, s) : launch_steps<BT, MM_F16, 8>(g, tm, s);
+}
+
+const char *const kMmaNames[2] = {"gemv_n_mma", "gemv_t_mma"};  // B row-major, B transposed
+
 }  // namespace
 
-int gemv_mma_config_count() { return 1; }
-const char *gemv_mma_config_name(int) { return "gemv_n_mma"; }
+int gemv_mma_config_count() { return 2; }
+const char *gemv_mma_config_name(int cfg) { return kMmaNames[cfg]; }
 
-bool gemv_mma_supports(const Problem &p, const DeviceInfo &d, int, std::string *why) {
+bool gemv_mma_supports(const Problem &p, const DeviceInfo &d, int cfg, std::string *why) {
   auto no = [&](const char *w) {
     if (why) *why = w;
     return false;
   };
   if (d.cc_major != 10) return no("needs an sm_10x device");
-  if (p.at || p.bt) return no("A and B must be row-major");
+  if (p.at) return no("A must be row-major");
+  if (p.bt != (cfg == 1)) return no(cfg == 1 ? "B must be transposed" : "B must be row-major");
   if (p.ta != p.tb || (p.ta != MM_BF16 && p.ta != MM_F16)) return no("A and B: both bf16 or both f16");
   if (p.M < 2 || p.M > 16) return no("M outside [2, 16]");
   if (p.N < 1 || p.K < 1) return no("empty problem");
   if (p.N >= (1LL << 30) || p.K >= (1LL << 30) || p.batch > 65535) return no("too large");
   if ((uintptr_t)p.B % 16 || (p.ldb * 2) % 16 || (p.batch > 1 && (p.sB * 2) % 16))
-    return no("B rows not 16-byte aligned");
+    return no("B's rows not 16-byte aligned");
   if ((uintptr_t)p.A % 8 || (p.lda * 2) % 8 || (p.batch > 1 && (p.sA * 2) % 8))
     return no("A rows not 8-byte aligned");
   if ((int64_t)d.smem_optin < (int64_t)kMmaSmem) return no("not enough shared memory");
@@ -410,7 +458,7 @@ bool gemv_mma_supports(const Problem &p, const DeviceInfo &d, int, std::string *
 mm_status launch_gemv_mma(const Problem &p, LaunchCtx &ctx, int cfg) {
   std::string why;
   if (!gemv_mma_supports(p, ctx.dev->info, cfg, &why))
-    return set_error(MM_ERR_UNSUPPORTED, "gemv_n_mma: %s", why.c_str());
+    return set_error(MM_ERR_UNSUPPORTED, "%s: %s", kMmaNames[cfg], why.c_str());
   MmaArgs g;
   std::memset(&g, 0, sizeof g);
   g.A = static_cast<const char *>(p.A);
@@ -444,14 +492,19 @@ mm_status launch_gemv_mma(const Problem &p, LaunchCtx &ctx, int cfg) {
   }
   const bool x16 = (uintptr_t)p.A % 16 == 0 && (p.lda * 2) % 16 == 0 &&
                    (p.batch == 1 || (p.sA * 2) % 16 == 0);
-  alignas(64) CUtensorMap tm;  // B, for the L2 prefetch boxes
-  mm_status st = encode_prefetch_map(&tm, p.tb, p.B, (uint64_t)p.N, (uint64_t)p.K,
-                                     (uint64_t)p.batch, (uint64_t)p.ldb * 2, (uint64_t)p.sB * 2,
-                                     kMmaCW, kPfRows);
+  // B, for the L2 prefetch boxes: [K][N] in boxes a group wide, or [N][K]
+  // in boxes of 256 k x 8 rows
+  alignas(64) CUtensorMap tm;
+  const bool bt = cfg == 1;
+  mm_status st = bt ? encode_prefetch_map(&tm, p.tb, p.B, (uint64_t)p.K, (uint64_t)p.N,
+                                          (uint64_t)p.batch, (uint64_t)p.ldb * 2,
+                                          (uint64_t)p.sB * 2, kPfTK, kPfTN)
+                    : encode_prefetch_map(&tm, p.tb, p.B, (uint64_t)p.N, (uint64_t)p.K,
+                                          (uint64_t)p.batch, (uint64_t)p.ldb * 2,
+                                          (uint64_t)p.sB * 2, kMmaCW, kPfRows);
   if (st != MM_OK) return st;
-  if (p.ta == MM_BF16)
-    return x16 ? launch_steps<MM_BF16, 16>(g, tm, ctx.stream) : launch_steps<MM_BF16, 8>(g, tm, ctx.stream);
-  return x16 ? launch_steps<MM_F16, 16>(g, tm, ctx.stream) : launch_steps<MM_F16, 8>(g, tm, ctx.stream);
+  return bt ? launch_types<true>(g, tm, p.ta, x16, ctx.stream)
+            : launch_types<false>(g, tm, p.ta, x16, ctx.stream);
 }
 
 }  // namespace mm

@@ -187,8 +187,9 @@ std::vector<PlanItem> make_plan(const KeyPod &k, const Problem &p, const DeviceI
 //   m = 1                  : gemv_n_stream / gemv_t_stream (B row-major / transposed)
 //   m <= 16, A and B       : gemv_n_mma (it also reads an A whose rows are only
 //     row-major              8-byte aligned in place)
-//   m <= 16 otherwise      : the swapped tensor-core split-K (on a copy of A if
-//                            A's rows are not 16-byte aligned)
+//   m <= 16, B transposed, : gemv_t_mma (A read in place), then the swapped
+//     A not 16-byte aligned  split-K on a copy of A
+//   m <= 16 otherwise      : the swapped tensor-core split-K
 //   few tiles, deep k      : split-K (the split-K group rule)
 //   f32 inputs             : tc_128x256_s4, tc_128x128_s6
 //   small outputs          : tc_128x64_s8 (m*n <= 512 x 512: latency)
@@ -200,7 +201,12 @@ std::vector<int> default_order(const KeyPod &k, const Problem &p, const DeviceIn
     pref = {p.bt ? "gemv_t_stream" : "gemv_n_stream"};
   } else if (k.m <= 16) {
     const char *swap = aligned_a ? "gemv_swap_tc_splitk_128x64_s8" : "gemv_swap_tc_repack_splitk_128x64";
-    pref = {"gemv_n_mma", swap};  // the first supports only row-major A and B
+    if (!p.bt)
+      pref = {"gemv_n_mma", swap};  // the first supports only row-major A and B
+    else if (!aligned_a)
+      pref = {"gemv_t_mma", swap};
+    else
+      pref = {swap, "gemv_t_mma"};
   } else if (prio_splitk(k, d) == PRIORITY_HIGH) {
     pref = {aligned_a ? "tc_splitk_128x128_s7" : "tc_repack_splitk_128x128"};
   } else if (p.ta == MM_F32) {

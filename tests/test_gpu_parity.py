@@ -103,6 +103,7 @@ def test_every_candidate_runs_somewhere():
         "gemv_n_stream": Case(1, 1000, 700, layout="NN", dist="int4"),
         "gemv_t_stream": Case(1, 1000, 704, layout="NT", dist="int4"),
         "gemv_n_mma": Case(16, 1000, 520, layout="NN", dt=(BF16, BF16, F32), dist="int4"),
+        "gemv_t_mma": Case(16, 1000, 520, layout="NT", dt=(BF16, BF16, F32), dist="int4"),
         "tc2_repack_256x256": Case(300, 264, 200, layout="NN", dist="int4", pad=(4, 0, 0)),
         "tc2_repack_256x224": Case(300, 264, 200, layout="NN", dist="int4", pad=(4, 0, 0)),
         "tc2_cpasync_256x256_s7": Case(300, 264, 200, layout="NN", dist="int4", pad=(4, 0, 0)),
@@ -301,20 +302,53 @@ def test_gemv_n_mma_shapes(shape_pad, dt):
     cr.check(exact=False)
 
 
+@pytest.mark.parametrize("shape_pad", [((16, 4096, 4096), (0, 0)), ((8, 4096, 4096), (4, 0)),
+                                       ((2, 1000, 700), (0, 4)), ((5, 70, 4100), (0, 4)),
+                                       ((16, 8, 20000), (0, 0)), ((13, 4104, 24), (4, 0)),
+                                       ((16, 264, 1000), (4, 0)), ((3, 1, 17), (3, 7))],
+                         ids=lambda s: "x".join(map(str, s[0])) + "+" + "_".join(map(str, s[1])))
+@pytest.mark.parametrize("dt", [(BF16, BF16, F32), (F16, F16, F16), (BF16, BF16, BF16)],
+                         ids=["bf16-f32", "f16-f16", "bf16-bf16"])
+def test_gemv_t_mma_shapes(shape_pad, dt):
+    """The warp-MMA small-M GEMV with B transposed (rows of n, k contiguous):
+    N ragged against the 64-row groups (down to one row), K ragged against
+    the 16-k chunks (zero-filled past K), B's rows padded to a multiple of
+    16 bytes, A padded to 8-byte rows, three launches in a row, a batch with
+    gaps, and a real-valued case."""
+    shape, (pa, pb) = shape_pad
+    i = NAMES.index("gemv_t_mma")
+    c = Case(*shape, layout="NT", dt=dt, dist="int4", pad=(pa, pb, 0), seed=sum(shape) + 1).device()
+    for _ in range(3):
+        c.device()
+        assert run(i, c) == mm.MM_OK, mm.mm_last_error()
+        c.check(exact=True)
+    # B's batch stride (295 * 904 + 896 + 16 elements) keeps 16-byte rows
+    cb = Case(7, 296, 896, layout="NT", dt=dt, dist="int4", batch=3, bstride_extra=(8, 16, 8),
+              pad=(4, 8, 4)).device()
+    assert run(i, cb) == mm.MM_OK, mm.mm_last_error()
+    cb.check(exact=True)
+    cr = Case(16, 4096, 4096, layout="NT", dt=dt, dist="normal", seed=19).device()
+    assert run(i, cr) == mm.MM_OK, mm.mm_last_error()
+    cr.check(exact=False)
+
+
 @pytest.mark.parametrize("shape_pad_batch", [((4, 128, 4096), (0, 0), 1), ((6, 1216, 8192), (4, 8), 1),
                                              ((3, 8192, 4096), (0, 0), 1), ((5, 256, 4096), (4, 0), 2)],
                          ids=lambda s: "x".join(map(str, s[0])) + "+" + "_".join(map(str, s[1])) +
                          f"+b{s[2]}")
 @pytest.mark.parametrize("dt", [(BF16, BF16, F32), (F16, F16, F16)], ids=["bf16-f32", "f16-f16"])
-def test_gemv_n_mma_even_splits(shape_pad_batch, dt):
+@pytest.mark.parametrize("cand,layout", [("gemv_n_mma", "NN"), ("gemv_t_mma", "NT")],
+                         ids=["n", "t"])
+def test_gemv_mma_even_splits(shape_pad_batch, dt, cand, layout):
     """Shapes whose K splits give every warp the same whole number of 16-row
     chunks and whose N is a whole number of 64-column groups, so the kernel
     runs its unchecked instance: with 152 SMs these take 2, 4, 16 and (with a
-    batch of two) 2 chunks a warp; A padded to 8-byte rows in two of them."""
+    batch of two) 2 chunks a warp; A padded to 8-byte rows in two of them;
+    B row-major and transposed."""
     shape, (pa, pb), batch = shape_pad_batch
-    i = NAMES.index("gemv_n_mma")
+    i = NAMES.index(cand)
     extra = (8, 16, 8) if batch > 1 else (0, 0, 0)
-    c = Case(*shape, layout="NN", dt=dt, dist="int4", pad=(pa, pb, 0), batch=batch,
+    c = Case(*shape, layout=layout, dt=dt, dist="int4", pad=(pa, pb, 0), batch=batch,
              bstride_extra=extra, seed=sum(shape) + batch).device()
     for _ in range(2):
         c.device()

@@ -211,10 +211,11 @@ SMALL_M_EXPECT = {  # candidates that must be among those run
     (1, "NT"): {"gemv_t", "gemv_t_stream", "gemv_t_rows", "gemv_swap_tc_splitk_128x64_s8"},
     (8, "NN"): {"gemv_n", "gemv_n_cluster", "gemv_n_mma", "gemv_swap_tc_splitk_128x64_s8",
                 "gemv_swap_tc_128x64_s8"},
-    (8, "NT"): {"gemv_t", "gemv_t_rows", "gemv_swap_tc_splitk_128x64_s8",
+    (8, "NT"): {"gemv_t", "gemv_t_rows", "gemv_t_mma", "gemv_swap_tc_splitk_128x64_s8",
                 "gemv_swap_tc_128x64_s8"},
     (16, "NN"): {"gemv_n", "gemv_n_mma", "gemv_swap_tc_splitk_128x64_s8", "gemv_swap_tc_128x64_s8"},
-    (16, "NT"): {"gemv_t", "gemv_swap_tc_splitk_128x64_s8", "gemv_swap_tc_128x64_s8"},
+    (16, "NT"): {"gemv_t", "gemv_t_mma", "gemv_swap_tc_splitk_128x64_s8",
+                 "gemv_swap_tc_128x64_s8"},
 }
 
 

@@ -185,7 +185,7 @@ def test_tuning_disabled_runs_default():
     ((16, 4096, 4096), "NN", 4, (BF16, BF16, BF16), None, "gemv_n_mma"),
     ((8, 4096, 4096), "NN", 0, (BF16, BF16, BF16), None, "gemv_n_mma"),
     ((8, 4096, 4096), "NT", 0, (BF16, BF16, BF16), None, "gemv_swap_tc_splitk_128x64_s8"),
-    ((16, 4096, 4096), "NT", 4, (BF16, BF16, BF16), None, "gemv_swap_tc_repack_splitk_128x64"),
+    ((16, 4096, 4096), "NT", 4, (BF16, BF16, BF16), None, "gemv_t_mma"),
     ((128, 128, 65536), "NN", 0, (BF16, BF16, BF16), None, "tc_splitk_128x128_s7"),
     ((4096, 4096, 4096), "NN", 0, (BF16, BF16, BF16), None, "tc2_256x256_s7"),
     ((8192, 4096, 4096), "NN", 4, (BF16, BF16, BF16), None, "tc2_repack_256x256"),
