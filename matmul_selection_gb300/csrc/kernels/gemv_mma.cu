@@ -20,12 +20,15 @@
 //       into L2, a few tensor-map boxes a CTA.
 //
 //   gemv_t_mma  the same with B transposed (stored [N][K], each output
-//       column a contiguous row of B): a chunk of B is then 64 rows of n x 32
-//       bytes of k, stored in shared memory as 32-byte rows with the two
-//       16-byte halves swapped on every other group of four rows (as A's
-//       tile), and read by plain ldmatrix, whose 8 x 8 matrices of (n, k)
-//       are exactly the MMA's "col" fragments of B.  Everything else is
-//       shared; B's L2 boxes are 256 k x 8 rows.
+//       column a contiguous row of B): a chunk of B is then one 32-row half
+//       of the group x 32 k (64 bytes a row, so a copy instruction touches 8
+//       rows), stored in shared memory as 64-byte rows with the 16-byte
+//       pieces XOR-swizzled by row pair, and read by plain ldmatrix, whose
+//       8 x 8 matrices of (n, k) are exactly the MMA's "col" fragments of B;
+//       two k steps of 16 a chunk, A's tile 16 x 32 k.  The warps' chunk
+//       stride (8) keeps each warp on one half, so a warp accumulates 32
+//       columns and the CTA adds the four warps of each half.  B's L2 boxes
+//       are 256 k x 8 rows.
 //
 // A need not be 16-byte aligned: its chunks are copied in 8-byte pieces when
 // its base or leading dimension is only 8-byte aligned (lda = 4100 bf16, for
@@ -49,6 +52,11 @@ constexpr int kMmaStages = 4;                    // chunks in flight a warp
 constexpr int kMmaStageB = 16 * kMmaRowB + 512;  // B's 16 rows, then A's 16 x 32 bytes
 constexpr int kMmaMaxSplits = 16;
 constexpr size_t kMmaSmem = (size_t)kMmaWarps * kMmaStages * kMmaStageB;
+// B transposed: a chunk is 32 rows of n x 32 k (64 bytes a row), then A's 16 x 64 bytes
+constexpr int kTRows = 32;
+constexpr int kTRowB = 64;
+constexpr int kTStageB = kTRows * kTRowB + 16 * kTRowB;
+constexpr size_t kMmaSmemT = (size_t)kMmaWarps * kMmaStages * kTStageB;
 
 struct MmaArgs {
   const char *A;
@@ -136,17 +144,19 @@ __device__ __forceinline__ int clampi(int v, int lo, int hi) { return v < lo ? l
 // 10.40 us a call at M = 16, 4096 x 4096, measured back to back); STEPS = 0:
 // a loop.  EVEN: every warp has exactly STEPS chunks, all inside K and every
 // group inside N (the host checks), so no copy needs a bound.  BT: B is
-// stored transposed ([N][K]).
+// stored transposed ([N][K]); its chunks are described at gemv_t_mma above.
 template <int TT, int XP, int STEPS, bool EVEN, bool BT>
 __global__ void __launch_bounds__(kMmaThreads, 2)
     gemv_mma_kernel(const MmaArgs g, const __grid_constant__ CUtensorMap tmB) {
   pdl_launch_dependents();
-  constexpr int NB = kMmaCW / 8;  // 8-column blocks of a group
+  constexpr int NB = (BT ? kTRows : kMmaCW) / 8;  // 8-column blocks a warp accumulates
+  constexpr int STB = BT ? kTStageB : kMmaStageB;  // bytes of a stage
+  constexpr int AOFF = BT ? kTRows * kTRowB : 16 * kMmaRowB;  // A's tile in a stage
   extern __shared__ __align__(128) uint8_t dsm[];
   __shared__ unsigned last;
   const int b = blockIdx.y;
   const int grp = blockIdx.x / g.S, sp = blockIdx.x - grp * g.S;
-  // the first crem splits take one chunk more (no division before the prefetch)
+  // the first crem splits take one 16-row unit more (no division before the prefetch)
   const int c0 = sp * g.cq + min(sp, g.crem), c1 = c0 + g.cq + (sp < g.crem ? 1 : 0);
   const int col0 = grp * kMmaCW;
   const char *Bb = g.B + (int64_t)b * g.sB * 2;
@@ -170,69 +180,103 @@ __global__ void __launch_bounds__(kMmaThreads, 2)
   }
   pdl_wait();  // A, the workspace, the tickets and C only after the previous kernel
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int mine = EVEN ? STEPS : c1 - c0 > warp ? (c1 - c0 - warp + kMmaWarps - 1) / kMmaWarps : 0;
-  uint8_t *wbase = dsm + (size_t)warp * kMmaStages * kMmaStageB;
-  // a group wholly inside N over whole 16-row chunks copies B unchecked
+  // the split's chunks: B row-major, one a 16-row unit; B transposed, two a
+  // pair of 16-k units (one for each 32-row half of the group; past an odd
+  // count's last unit zero-filled).  Warp w takes chunks w, w + 8, ...: with
+  // B transposed always the same half, w % 2.
+  const int nun = BT ? 2 * ((c1 - c0 + 1) >> 1) : c1 - c0;
+  const int mine = EVEN ? STEPS : nun > warp ? (nun - warp + kMmaWarps - 1) / kMmaWarps : 0;
+  const int half = warp & 1;
+  const int kend = min(g.K, c1 * 16);  // no k past the split is read
+  uint8_t *wbase = dsm + (size_t)warp * kMmaStages * STB;
+  // a group wholly inside N over whole 16-row units copies B unchecked
   const bool b_whole = EVEN || (col0 + kMmaCW <= g.N && g.K % 16 == 0);
   // copies of the warp's i-th chunk into stage i % kMmaStages (an empty group
   // past the last chunk keeps the wait counts uniform)
   auto issue = [&](int i) {
     if (i < mine) {
-      const int c = c0 + warp + i * kMmaWarps;
-      const uint32_t dst = smem_addr(wbase + (size_t)(i % kMmaStages) * kMmaStageB);
+      const int c = warp + i * kMmaWarps;  // within the split
+      const uint32_t dst = smem_addr(wbase + (size_t)(i % kMmaStages) * STB);
       if constexpr (BT) {
-        // B: 64 rows of n x 2 pieces (k 16c .. 16c + 7, + 8 .. + 15); lane:
-        // piece lane % 2 of rows lane / 2 + 16 j
-        const int k = c * 16 + (lane & 1) * 8;
+        const int k0 = (c0 + 2 * (c >> 1)) * 16;
+        const bool whole = b_whole && (EVEN || k0 + 32 <= kend);
+        // B: the half's 32 rows of n x 4 pieces of 8 k (64 bytes, k0 .. k0 +
+        // 31); lane: piece lane % 4 of rows lane / 4 + 8 j
+        const int p = lane & 3, k = k0 + p * 8;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          const int row = (lane >> 1) + 16 * j, h = lane & 1, n = col0 + row;
-          const uint32_t d = dst + row * 32 + ((h ^ ((row >> 2) & 1)) << 4);
-          if (b_whole) {
+          const int row = (lane >> 2) + 8 * j, n = col0 + half * kTRows + row;
+          const uint32_t d = dst + row * kTRowB + ((p ^ ((row >> 1) & 3)) << 4);
+          if (whole) {
             cp16(d, Bb + ((int64_t)n * g.ldb + k) * 2, 16u);
           } else {
-            const int valid = n < g.N ? clampi(g.K - k, 0, 8) * 2 : 0;
+            const int valid = n < g.N ? clampi(kend - k, 0, 8) * 2 : 0;
             cp16(d, valid ? Bb + ((int64_t)n * g.ldb + k) * 2 : g.B, (uint32_t)valid);
           }
         }
-      } else if (b_whole) {
-        // B: 16 rows x 8 pieces; lane: pieces lane % 8 of rows lane / 8 + 4 j
-        const char *src = Bb + ((int64_t)(c * 16 + lane / 8) * g.ldb + col0 + (lane % 8) * 8) * 2;
-        const int64_t step4 = 4 * g.ldb * 2;
+        // A: rows below M of the 16 x 64-byte tile at the same k
+        if constexpr (XP == 16) {
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int row = lane / 8 + 4 * j, piece = lane % 8;
-          cp16(dst + row * kMmaRowB + ((piece ^ (row & 7)) << 4), src + j * step4, 16u);
+          for (int j = 0; j < 2; ++j) {
+            const int e = lane + 32 * j, m = e >> 2, q = e & 3, ka = k0 + q * 8;
+            if (m < g.M) {
+              const int valid = whole ? 16 : clampi(kend - ka, 0, 8) * 2;
+              cp16(dst + AOFF + m * kTRowB + ((q ^ ((m >> 1) & 3)) << 4),
+                   valid ? Ab + ((int64_t)m * g.lda + ka) * 2 : g.A, (uint32_t)valid);
+            }
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int e = lane + 32 * j, m = e >> 3, q = e & 7, ka = k0 + q * 4;
+            if (m < g.M) {
+              const int valid = whole ? 8 : clampi(kend - ka, 0, 4) * 2;
+              cp8(dst + AOFF + m * kTRowB + (((q >> 1) ^ ((m >> 1) & 3)) << 4) + (q & 1) * 8,
+                  valid ? Ab + ((int64_t)m * g.lda + ka) * 2 : g.A, (uint32_t)valid);
+            }
+          }
         }
       } else {
+        const int cu = c0 + c;  // the 16-row unit
+        if (b_whole) {
+          // B: 16 rows x 8 pieces; lane: pieces lane % 8 of rows lane / 8 + 4 j
+          const char *src = Bb + ((int64_t)(cu * 16 + lane / 8) * g.ldb + col0 + (lane % 8) * 8) * 2;
+          const int64_t step4 = 4 * g.ldb * 2;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int row = lane / 8 + 4 * j, piece = lane % 8;
-          const int r = c * 16 + row, n = col0 + piece * 8;
-          const int valid = r < g.K ? clampi(g.N - n, 0, 8) * 2 : 0;
-          const char *src = valid ? Bb + ((int64_t)r * g.ldb + n) * 2 : g.B;
-          cp16(dst + row * kMmaRowB + ((piece ^ (row & 7)) << 4), src, (uint32_t)valid);
-        }
-      }
-      // A: rows below M of the 16 x 32-byte tile (k = 16c .. 16c + 15), k
-      // past K zero; the rows from M on were cleared once
-      const int k0 = c * 16;
-      if constexpr (XP == 16) {
-        const int m = lane >> 1, h = lane & 1;
-        if (m < g.M) {
-          const int valid = EVEN ? 16 : clampi(g.K - (k0 + 8 * h), 0, 8) * 2;
-          const char *src = valid ? Ab + ((int64_t)m * g.lda + k0 + 8 * h) * 2 : g.A;
-          cp16(dst + 16 * kMmaRowB + m * 32 + ((h ^ ((m >> 2) & 1)) << 4), src, (uint32_t)valid);
-        }
-      } else {
+          for (int j = 0; j < 4; ++j) {
+            const int row = lane / 8 + 4 * j, piece = lane % 8;
+            cp16(dst + row * kMmaRowB + ((piece ^ (row & 7)) << 4), src + j * step4, 16u);
+          }
+        } else {
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          const int e = lane + 32 * j, m = e >> 2, q = e & 3, h = q >> 1;
+          for (int j = 0; j < 4; ++j) {
+            const int row = lane / 8 + 4 * j, piece = lane % 8;
+            const int r = cu * 16 + row, n = col0 + piece * 8;
+            const int valid = r < g.K ? clampi(g.N - n, 0, 8) * 2 : 0;
+            const char *src = valid ? Bb + ((int64_t)r * g.ldb + n) * 2 : g.B;
+            cp16(dst + row * kMmaRowB + ((piece ^ (row & 7)) << 4), src, (uint32_t)valid);
+          }
+        }
+        // A: rows below M of the 16 x 32-byte tile (k = 16 cu .. + 15), k
+        // past K zero
+        const int k0 = cu * 16;
+        if constexpr (XP == 16) {
+          const int m = lane >> 1, h = lane & 1;
           if (m < g.M) {
-            const int valid = EVEN ? 8 : clampi(g.K - (k0 + 4 * q), 0, 4) * 2;
-            const char *src = valid ? Ab + ((int64_t)m * g.lda + k0 + 4 * q) * 2 : g.A;
-            cp8(dst + 16 * kMmaRowB + m * 32 + ((h ^ ((m >> 2) & 1)) << 4) + (q & 1) * 8, src,
-                (uint32_t)valid);
+            const int valid = EVEN ? 16 : clampi(g.K - (k0 + 8 * h), 0, 8) * 2;
+            const char *src = valid ? Ab + ((int64_t)m * g.lda + k0 + 8 * h) * 2 : g.A;
+            cp16(dst + AOFF + m * 32 + ((h ^ ((m >> 2) & 1)) << 4), src, (uint32_t)valid);
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            const int e = lane + 32 * j, m = e >> 2, q = e & 3, h = q >> 1;
+            if (m < g.M) {
+              const int valid = EVEN ? 8 : clampi(g.K - (k0 + 4 * q), 0, 4) * 2;
+              const char *src = valid ? Ab + ((int64_t)m * g.lda + k0 + 4 * q) * 2 : g.A;
+              cp8(dst + AOFF + m * 32 + ((h ^ ((m >> 2) & 1)) << 4) + (q & 1) * 8, src,
+                  (uint32_t)valid);
+            }
           }
         }
       }
@@ -240,15 +284,17 @@ __global__ void __launch_bounds__(kMmaThreads, 2)
     cp_commit();
   };
   // A's rows from M on (the MMA's rows past the problem) zero in every stage,
-  // cleared once here and never copied: 32 bytes a row, whatever the swizzle
+  // cleared once here and never copied: whole rows, whatever the swizzle
   if (g.M < 16) {
+    constexpr int APIECES = BT ? 16 * kTRowB / 16 : 16 * 32 / 16;  // 16-byte pieces of A's tile
 #pragma unroll
-    for (int st = 0; st < kMmaStages; ++st) {
-      const int m = lane >> 1;
-      if (m >= g.M)
-        *reinterpret_cast<uint4 *>(wbase + (size_t)st * kMmaStageB + 16 * kMmaRowB + lane * 16) =
-            make_uint4(0u, 0u, 0u, 0u);
-    }
+    for (int st = 0; st < kMmaStages; ++st)
+#pragma unroll
+      for (int e = lane; e < APIECES; e += 32) {
+        const int m = e / (APIECES / 16);
+        if (m >= g.M)
+          *reinterpret_cast<uint4 *>(wbase + (size_t)st * STB + AOFF + e * 16) = make_uint4(0u, 0u, 0u, 0u);
+      }
     __syncwarp();  // ordered before any lane's fragment loads
   }
 #pragma unroll
@@ -260,29 +306,45 @@ __global__ void __launch_bounds__(kMmaThreads, 2)
     for (int q = 0; q < 4; ++q) acc[nb][q] = 0.f;
   // one chunk: its fragments and MMAs
   auto compute = [&](int i) {
-    const uint32_t base = smem_addr(wbase + (size_t)(i % kMmaStages) * kMmaStageB);
-    // A's fragments: matrices (m 0-7, k 0-7), (m 8-15, k 0-7), (m 0-7, k 8-15), (m 8-15, k 8-15)
-    uint32_t a[4];
-    {
-      const int mat = lane >> 3, r = lane & 7;
-      const int m = (mat & 1) * 8 + r, h = mat >> 1;
-      ldm_x4(base + 16 * kMmaRowB + m * 32 + ((h ^ ((m >> 2) & 1)) << 4), a[0], a[1], a[2], a[3]);
-    }
-    // B's fragments, two column blocks an ldmatrix: matrices (k 0-7, block),
-    // (k 8-15, block), (k 0-7, block + 1), (k 8-15, block + 1)
+    const uint32_t base = smem_addr(wbase + (size_t)(i % kMmaStages) * STB);
+    const int mat = lane >> 3, r = lane & 7;
+    if constexpr (BT) {
+      // two k steps of 16; A's matrices (m 0-7, k lo), (m 8-15, k lo), (m 0-7,
+      // k hi), (m 8-15, k hi); B's (block, k lo), (block, k hi), (block + 1,
+      // k lo), (block + 1, k hi), rows of n read without a transpose
 #pragma unroll
-    for (int nb = 0; nb < NB; nb += 2) {
-      const int mat = lane >> 3, r = lane & 7;
-      uint32_t b0, b1, b2, b3;
-      if constexpr (BT) {  // rows of n, 8 k a matrix row: no transpose
-        const int nrow = (nb + (mat >> 1)) * 8 + r, h = mat & 1;
-        ldm_x4(base + nrow * 32 + ((h ^ ((nrow >> 2) & 1)) << 4), b0, b1, b2, b3);
-      } else {
-        const int krow = (mat & 1) * 8 + r, piece = nb + (mat >> 1);
-        ldm_x4_trans(base + krow * kMmaRowB + ((piece ^ (krow & 7)) << 4), b0, b1, b2, b3);
+      for (int s = 0; s < 2; ++s) {
+        uint32_t a[4];
+        {
+          const int m = (mat & 1) * 8 + r, q = 2 * s + (mat >> 1);
+          ldm_x4(base + AOFF + m * kTRowB + ((q ^ ((m >> 1) & 3)) << 4), a[0], a[1], a[2], a[3]);
+        }
+#pragma unroll
+        for (int nb = 0; nb < NB; nb += 2) {
+          const int nrow = (nb + (mat >> 1)) * 8 + r, q = 2 * s + (mat & 1);
+          uint32_t b0, b1, b2, b3;
+          ldm_x4(base + nrow * kTRowB + ((q ^ ((nrow >> 1) & 3)) << 4), b0, b1, b2, b3);
+          mma_16816<TT>(acc[nb], a, b0, b1);
+          mma_16816<TT>(acc[nb + 1], a, b2, b3);
+        }
       }
-      mma_16816<TT>(acc[nb], a, b0, b1);
-      mma_16816<TT>(acc[nb + 1], a, b2, b3);
+    } else {
+      // A's fragments: matrices (m 0-7, k 0-7), (m 8-15, k 0-7), (m 0-7, k 8-15), (m 8-15, k 8-15)
+      uint32_t a[4];
+      {
+        const int m = (mat & 1) * 8 + r, h = mat >> 1;
+        ldm_x4(base + AOFF + m * 32 + ((h ^ ((m >> 2) & 1)) << 4), a[0], a[1], a[2], a[3]);
+      }
+      // B's fragments, two column blocks an ldmatrix: matrices (k 0-7, block),
+      // (k 8-15, block), (k 0-7, block + 1), (k 8-15, block + 1)
+#pragma unroll
+      for (int nb = 0; nb < NB; nb += 2) {
+        const int krow = (mat & 1) * 8 + r, piece = nb + (mat >> 1);
+        uint32_t b0, b1, b2, b3;
+        ldm_x4_trans(base + krow * kMmaRowB + ((piece ^ (krow & 7)) << 4), b0, b1, b2, b3);
+        mma_16816<TT>(acc[nb], a, b0, b1);
+        mma_16816<TT>(acc[nb + 1], a, b2, b3);
+      }
     }
   };
   if constexpr (STEPS > 0) {
@@ -305,31 +367,39 @@ __global__ void __launch_bounds__(kMmaThreads, 2)
   }
   cp_wait<0>();
   __syncwarp();
-  // the warp's 16 x 64 sums into its own stages (no copy is in flight there)
+  // the warp's sums into its own stages (no copy is in flight there): all 64
+  // columns, or with B transposed its half's 32
   constexpr int PLD = kMmaCW + 1;
-  static_assert(kMmaStages * kMmaStageB >= 16 * PLD * 4, "a warp's sums fit its stages");
+  static_assert(kMmaStages * STB >= 16 * PLD * 4, "a warp's sums fit its stages");
   {
     float *pw = reinterpret_cast<float *>(wbase);
-    const int gr = lane >> 2, t = lane & 3;
+    const int gr = lane >> 2, t = lane & 3, cb = BT ? half * kTRows : 0;
 #pragma unroll
     for (int nb = 0; nb < NB; ++nb) {
-      pw[gr * PLD + nb * 8 + 2 * t] = acc[nb][0];
-      pw[gr * PLD + nb * 8 + 2 * t + 1] = acc[nb][1];
-      pw[(gr + 8) * PLD + nb * 8 + 2 * t] = acc[nb][2];
-      pw[(gr + 8) * PLD + nb * 8 + 2 * t + 1] = acc[nb][3];
+      pw[gr * PLD + cb + nb * 8 + 2 * t] = acc[nb][0];
+      pw[gr * PLD + cb + nb * 8 + 2 * t + 1] = acc[nb][1];
+      pw[(gr + 8) * PLD + cb + nb * 8 + 2 * t] = acc[nb][2];
+      pw[(gr + 8) * PLD + cb + nb * 8 + 2 * t + 1] = acc[nb][3];
     }
   }
   __syncthreads();
-  // the CTA's sums, warps added in order: 16 x 64 outputs, 4 a thread
+  // the CTA's sums, warps added in order (with B transposed the four warps
+  // of the column's half): 16 x 64 outputs, 4 a thread
   constexpr int OPT = 16 * kMmaCW / kMmaThreads;
   float tv[OPT];
 #pragma unroll
   for (int j = 0; j < OPT; ++j) {
     const int o = threadIdx.x + j * kMmaThreads, m = o / kMmaCW, n = o % kMmaCW;
     float s = 0.f;
+    if constexpr (BT) {
 #pragma unroll
-    for (int w = 0; w < kMmaWarps; ++w)
-      s += reinterpret_cast<const float *>(dsm + (size_t)w * kMmaStages * kMmaStageB)[m * PLD + n];
+      for (int w = n / kTRows; w < kMmaWarps; w += 2)
+        s += reinterpret_cast<const float *>(dsm + (size_t)w * kMmaStages * STB)[m * PLD + n];
+    } else {
+#pragma unroll
+      for (int w = 0; w < kMmaWarps; ++w)
+        s += reinterpret_cast<const float *>(dsm + (size_t)w * kMmaStages * STB)[m * PLD + n];
+    }
     tv[j] = s;
   }
   auto store = [&](int o, float v) {
@@ -380,10 +450,13 @@ void mma_plan(int64_t N, int64_t K, int64_t batch, int sms, int *G, int *S) {
   *S = (int)std::max<int64_t>(1, s);
 }
 
-// Unrolled steps for the most chunks a warp gets: 2, 4, 8 or 16, else 0 (a loop).
-int mma_steps(const MmaArgs &g) {
+// Unrolled steps for the most chunks a warp gets: 2, 4, 8 or 16, else 0 (a
+// loop).  A split of u 16-row units has u chunks, or with B transposed 2 *
+// ceil(u / 2).
+int mma_steps(const MmaArgs &g, bool bt) {
   const int nch = (g.K + 15) / 16, per_split = (nch + g.S - 1) / g.S;
-  const int per_warp = (per_split + kMmaWarps - 1) / kMmaWarps;
+  const int chunks = bt ? 2 * ((per_split + 1) / 2) : per_split;
+  const int per_warp = (chunks + kMmaWarps - 1) / kMmaWarps;
   return per_warp <= 2 ? 2 : per_warp <= 4 ? 4 : per_warp <= 8 ? 8 : per_warp <= 16 ? 16 : 0;
 }
 
@@ -392,12 +465,13 @@ mm_status launch_mma(const MmaArgs &g, const CUtensorMap &tm, cudaStream_t s) {
   auto kern = gemv_mma_kernel<TT, XP, STEPS, EVEN, BT>;
   static std::once_flag once;
   static cudaError_t attr = cudaSuccess;
+  constexpr size_t smem = BT ? kMmaSmemT : kMmaSmem;
   std::call_once(once, [&] {
-    attr = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kMmaSmem);
+    attr = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   });
   if (attr != cudaSuccess) return cuda_error(attr, "gemv_mma shared memory attribute");
   cudaError_t e = launch_pdl(kern, dim3((unsigned)(g.G * g.S), (unsigned)g.batch),
-                             dim3(kMmaThreads), kMmaSmem, s, dim3(1), g, tm);
+                             dim3(kMmaThreads), smem, s, dim3(1), g, tm);
   return e == cudaSuccess ? MM_OK : cuda_error(e, "gemv_mma launch");
 }
 
@@ -412,7 +486,7 @@ mm_status launch_steps(const MmaArgs &g, const CUtensorMap &tm, cudaStream_t s) 
     case 16: return launch_mma<BT, TT, XP, 16, true>(g, tm, s);
     default: break;
     }
-  switch (mma_steps(g)) {
+  switch (mma_steps(g, BT)) {
   case 2: return launch_mma<BT, TT, XP, 2>(g, tm, s);
   case 4: return launch_mma<BT, TT, XP, 4>(g, tm, s);
   case 8: return launch_mma<BT, TT, XP, 8>(g, tm, s);
@@ -451,7 +525,8 @@ bool gemv_mma_supports(const Problem &p, const DeviceInfo &d, int cfg, std::stri
     return no("B's rows not 16-byte aligned");
   if ((uintptr_t)p.A % 8 || (p.lda * 2) % 8 || (p.batch > 1 && (p.sA * 2) % 8))
     return no("A rows not 8-byte aligned");
-  if ((int64_t)d.smem_optin < (int64_t)kMmaSmem) return no("not enough shared memory");
+  if ((int64_t)d.smem_optin < (int64_t)(cfg == 1 ? kMmaSmemT : kMmaSmem))
+    return no("not enough shared memory");
   return true;
 }
 
