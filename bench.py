@@ -258,7 +258,7 @@ def ensure_built():
 def kernel_sources(kernel_name):
     """The source files that hold a candidate's kernels."""
     kdir = os.path.join(ROOT, "matmul_selection_gb300", "csrc", "kernels")
-    if kernel_name.startswith(("tc_repack", "tc2_repack")):
+    if kernel_name.startswith(("tc_repack", "tc2_repack", "gemv_swap_tc_repack")):
         names = ["repack.cu", "tc_gemm.cu"]
     elif kernel_name.startswith(("tc", "gemv_swap_tc")):
         names = ["tc_gemm.cu"]

@@ -41,3 +41,23 @@ def test_two_rank_max_and_aggregate():
 def test_single_rank_is_identity():
     assert bench.max_over_ranks(3.5, 1, "cpu") == 3.5
     assert bench.aggregate_rate(10.0, 1, 2.0) == 5.0
+
+
+def test_kernel_sources_cover_each_candidate():
+    """bench.py trusts a candidate's committed ncu counters only while the
+    hash of that candidate's kernel sources is unchanged, so each candidate
+    must map to the file that defines it: where a candidate's name is a
+    string literal in kernel files (its configuration table, or a table
+    that refers to it), at least one of them is among the files hashed."""
+    import re
+
+    import matmul_selection_gb300 as mm
+
+    kdir = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                        "matmul_selection_gb300", "csrc", "kernels")
+    texts = {f: open(os.path.join(kdir, f)).read() for f in os.listdir(kdir) if f.endswith(".cu")}
+    for name in mm.candidate_names():
+        hashed = {os.path.basename(p) for p in bench.kernel_sources(name)}
+        assert hashed and all(os.path.exists(os.path.join(kdir, f)) for f in hashed), name
+        defining = {f for f, t in texts.items() if re.search(r'"%s"' % re.escape(name), t)}
+        assert not defining or defining & hashed, (name, sorted(defining), sorted(hashed))
